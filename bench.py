@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the hyper-connection low-rank mix block on GB300.
+
+Default workload: the single decode block (rows = 1, C = 4, H = 2560, R = 320,
+bf16, with prologue, the Qwen-shaped attributes), run as a chain over 96
+distinct synthetic weight sets (1.27 GB of weights, far larger than the 129 MB
+L2, so every block reads its weights from HBM). Block i + 1 takes block i's
+pre_output and post_gate as its prologue and its streams_out as streams. One
+step = one block. The timed steps replay CUDA graphs of 96 (and a remainder
+of) chained blocks, captured from the public API; their kernels are linked by
+programmatic dependent launch.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle
+instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "µs/block and rows/s, rows 1–8192, as % of HBM / bf16 tensor roofline"
+C, H, R = 4, 2560, 320
+NSETS = 96
+QWEN = dict(epsilon=1e-6, reduction_scale=0.25, silu_alpha=0.25, gate_div=4.0, gate_mul=2.0)
+WORKLOAD = ("decode block: rows=1, C=4, H=2560, R=320, bf16, with prologue, Qwen attributes; "
+            "chain over 96 distinct weight sets (1.27 GB), graph replay")
+
+
+def block_bytes(rows, C, H, R, es, prologue=True):
+    """Algorithmic bytes of one block: weights and norm_scale once, and per row
+    streams in, streams_out, prev_out, prev_gate, pre_output, post_gate."""
+    CH = C * H
+    weights = (2 * CH * R + CH * C + CH) * es
+    per_row = (2 * CH + H + C + (H + C if prologue else 0)) * es
+    return weights + rows * per_row
+
+
+def block_flops(rows, C, H, R):
+    CH = C * H
+    return 2 * rows * (2 * CH * R + CH * C)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return dict(hbm=float(j["hbm_gbs"]), bf16=float(j["bf16_tflops"]),
+                    bf16_sustained=float(j.get("bf16_tflops_sustained", j["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "hyper_connection_rank_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(name):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    j = json.load(open(p)).get(name)
+    if not j or j.get("source_hash") != kernel_source_hash():
+        return None
+    return j.get("dram_bytes_per_unit")
+
+
+# ------------------------------------------------------------ clocks --
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.p = None
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                       "-lms", "100", "-i", str(gpu_index)], stdout=subprocess.PIPE,
+                                      stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ our arm --
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import __graft_entry__
+    import hyper_connection_rank_gb300 as hc
+    from hyper_connection_rank_gb300 import inputs as I
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    __graft_entry__.build()
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+
+    def barrier():
+        if dist:
+            tdist.barrier()
+
+    rows = 1
+    flags = hc.HC_FLAG_WEIGHTS_STATIC
+    assert hc.path(rows, C, H, R, torch.bfloat16, flags) == hc.HC_PATH_DECODE
+    weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(NSETS)]
+    bufs = [I.make_activations(rows, C, H, "bf16", seed=0, block=0, prologue=True, device=dev)]
+    bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
+    ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        src, dst, w = bufs[i % 2], bufs[(i + 1) % 2], weights[i % NSETS]
+        hc.lowrank_mix(src["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], src["prev_out"],
+                       src["prev_gate"], num_branches=C, flags=flags,
+                       out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
+
+    def capture(n):
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(dev)
+        s.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n):
+                    step(i)
+        torch.cuda.current_stream(dev).wait_stream(s)
+        return g
+
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    g_full = capture(NSETS) if K >= NSETS else None
+    g_rem = capture(K % NSETS) if K % NSETS else None
+    torch.cuda.synchronize()
+
+    stream = torch.cuda.current_stream(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(K // NSETS):
+        g_full.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop() if sampler else None
+    t_ms = ev0.elapsed_time(ev1)
+    if dist:
+        tt = torch.tensor([t_ms], device=dev)
+        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
+        t_ms = float(tt.item())
+    for b in bufs:
+        for v in b.values():
+            assert torch.isfinite(v.float()).all(), "non-finite values in the chain"
+
+    us_per_block = 1000.0 * t_ms / K
+    value = world * rows * K / (t_ms / 1000.0)
+    pk = peaks()
+    bytes_blk = block_bytes(rows, C, H, R, 2)
+    achieved = bytes_blk / (us_per_block * 1e-6) / 1e9
+    traffic = recorded_traffic("decode_block_rows1_bf16")
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "rows/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": t_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; Qwen-shaped, random weights)",
+        "config": {"workload": WORKLOAD, "rows": rows, "C": C, "H": H, "R": R, "weight_sets": NSETS,
+                   "l2": "inputs larger than L2: 96 weight sets of 13.2 MB rotated (1.27 GB)",
+                   "parallelism": f"replicas x{world}"},
+        "us_per_block": round(us_per_block, 4),
+        "roofline": {"bound": "hbm", "kernel": "decode block (dec_down + dec_up, PDL-overlapped)",
+                     "achieved": round(achieved, 1), "peak": pk["hbm"], "unit": "GB/s",
+                     "frac": round(achieved / pk["hbm"], 4), "peak_source": pk["source"],
+                     "bytes_per_launch": bytes_blk, "traffic": traffic},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_e2e:
+        result["e2e"] = e2e_measure(args, hc, I, weights, dev, flags)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    if rank == 0 and not args.no_sweep:
+        del weights
+        torch.cuda.empty_cache()
+        result["sweep"] = sweep(hc, I, dev, pk)
+    return result
+
+
+def e2e_measure(args, hc, I, weights, dev, flags):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs host->device from pinned memory, runs the block, and reads its
+    outputs back device->host."""
+    import torch
+    rows = 1
+    src = I.make_activations(rows, C, H, "bf16", seed=1, block=0, prologue=True, device="cpu")
+    host_in = {k: v.pin_memory() for k, v in src.items()}
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in src.items()}
+    dev_out = (torch.empty(rows, H, dtype=torch.bfloat16, device=dev),
+               torch.empty(rows, C, dtype=torch.bfloat16, device=dev),
+               torch.empty(rows, C * H, dtype=torch.bfloat16, device=dev))
+    host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out)
+    ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
+    n = max(1, min(args.steps, args.e2e_steps))
+
+    def one(i):
+        for k in ("streams", "prev_out", "prev_gate"):
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        w = weights[i % NSETS]
+        hc.lowrank_mix(dev_in["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
+                       dev_in["prev_out"], dev_in["prev_gate"], num_branches=C, flags=flags, out=dev_out,
+                       workspace=ws, **QWEN)
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+
+    for i in range(max(3, args.warmup)):
+        one(i)
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    e0.record(s)
+    for i in range(n):
+        one(i)
+    e1.record(s)
+    e1.synchronize()
+    wall = time.perf_counter() - t0
+    t = e0.elapsed_time(e1) / 1000.0
+    bi = sum(v.numel() * v.element_size() for v in host_in.values())
+    bo = sum(v.numel() * v.element_size() for v in host_out)
+    return {"value": round(rows * n / t, 1), "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+            "steps": n, "us_per_step": round(1e6 * t / n, 3), "wall_us_per_step": round(1e6 * wall / n, 3),
+            "api": "hyper_connection_rank_gb300.lowrank_mix -> hc_lowrank_mix (C ABI), eager launches"}
+
+
+def cpu_baseline(seconds):
+    """The oracle, as it stands, on a bounded sample of the workload: chained
+    rows=1 bf16 blocks over 2 weight sets, single-threaded (one row cannot be
+    split across threads by the oracle), for about `seconds` of CPU time."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from hyper_connection_rank_gb300 import inputs as I
+    oracle.build()
+    codes = lambda t: None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ws = [I.make_weights(C, H, R, "bf16", seed=0, block=i) for i in range(2)]
+    ws = [{k: codes(v) for k, v in w.items()} for w in ws]
+    act = {k: codes(v) for k, v in I.make_activations(1, C, H, "bf16", seed=0, block=0, prologue=True).items()}
+    n, t0 = 0, time.perf_counter()
+    while True:
+        w = ws[n % 2]
+        pre, post, sout = oracle.lowrank_mix(act["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
+                                             act["prev_out"], act["prev_gate"], num_branches=C,
+                                             dtype=oracle.DT_BF16, nthreads=1, **QWEN)
+        act = {"streams": sout, "prev_out": pre, "prev_gate": post}
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and n >= 3) or n >= 100000:
+            break
+    return {"value": round(n / el, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} chained decode blocks (rows=1, bf16, C=4, H=2560, R=320) over 2 weight sets, "
+                      f"{el:.1f} s on 1 host thread", "us_per_block": round(1e6 * el / n, 1)}
+
+
+def sweep(hc, I, dev, pk):
+    """Other configurations of the metric (context lines, not the headline):
+    decode rows 1/2/4/8 in bf16 and fp16 (96-block graphs; us/block also as the
+    slope between 96- and 48-block graphs, min over 15 x 10 replays), and the
+    8192-row prefill blocks."""
+    import torch
+    out = {}
+    flags = hc.HC_FLAG_WEIGHTS_STATIC
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        weights = [I.make_weights(C, H, R, dt, seed=0, block=i, device=dev) for i in range(NSETS)]
+        for rows in (1, 2, 4, 8):
+            bufs = [I.make_activations(rows, C, H, dt, seed=0, block=0, prologue=True, device=dev)]
+            bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
+            ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, tdt, flags)), dtype=torch.uint8, device=dev)
+
+            def step(i):
+                src, dst, w = bufs[i % 2], bufs[(i + 1) % 2], weights[i % NSETS]
+                hc.lowrank_mix(src["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
+                               src["prev_out"], src["prev_gate"], num_branches=C, flags=flags,
+                               out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
+
+            graphs = {}
+            for n in (96, 48):
+                step(0)
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream(dev)
+                s.wait_stream(torch.cuda.current_stream(dev))
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for i in range(n):
+                            step(i)
+                torch.cuda.current_stream(dev).wait_stream(s)
+                graphs[n] = g
+            best = {}
+            for n, g in graphs.items():
+                g.replay()
+                torch.cuda.synchronize()
+                ts = []
+                for _ in range(15):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    for _ in range(10):
+                        g.replay()
+                    e1.record()
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) / 10)
+                best[n] = min(ts)
+            us96 = 1000 * best[96] / 96
+            slope = 1000 * (best[96] - best[48]) / 48
+            b = block_bytes(rows, C, H, R, 2)
+            out[f"decode_rows{rows}_{dt}"] = {
+                "us_per_block": round(us96, 3), "us_per_block_slope": round(slope, 3),
+                "rows_per_s": round(rows / (us96 * 1e-6), 1),
+                "hbm_frac": round(b / (us96 * 1e-6) / 1e9 / pk["hbm"], 4),
+                "hbm_frac_slope": round(b / (slope * 1e-6) / 1e9 / pk["hbm"], 4) if slope > 0 else None}
+            del graphs
+        del weights
+        torch.cuda.empty_cache()
+    for dt, tdt, Cp, Hp in (("bf16", torch.bfloat16, 4, 2560), ("f16", torch.float16, 8, 1280)):
+        rows = 8192
+        d = I.make_block(rows, Cp, Hp, R, dt, seed=0, prologue=True, device=dev)
+        pre = torch.empty(rows, Hp, dtype=tdt, device=dev)
+        post = torch.empty(rows, Cp, dtype=tdt, device=dev)
+        sout = torch.empty(rows, Cp * Hp, dtype=tdt, device=dev)
+        ws = torch.empty(max(1, hc.workspace_size(rows, Cp, Hp, R, tdt)), dtype=torch.uint8, device=dev)
+
+        def call():
+            hc.lowrank_mix(d["streams"], d["norm_scale"], d["down_w"], d["up_w"], d["inject_w"], d["prev_out"],
+                           d["prev_gate"], num_branches=Cp, out=(pre, post, sout), workspace=ws, **QWEN)
+
+        for _ in range(3):
+            call()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(10):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            call()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        t = min(ts) / 1000
+        b, f = block_bytes(rows, Cp, Hp, R, 2), block_flops(rows, Cp, Hp, R)
+        t_roof = max(b / (pk["hbm"] * 1e9), f / (pk["bf16"] * 1e12))
+        out[f"prefill_rows{rows}_C{Cp}_H{Hp}_{dt}"] = {
+            "path": hc.PATH_NAMES[hc.path(rows, Cp, Hp, R, tdt)],
+            "us_per_block": round(1e6 * t, 2), "us_per_block_median": round(1e3 * statistics.median(ts), 2),
+            "rows_per_s": round(rows / t, 1), "hbm_frac": round(b / t / 1e9 / pk["hbm"], 4),
+            "tensor_frac": round(f / t / 1e12 / pk["bf16"], 4), "roofline_frac": round(t_roof / t, 4)}
+        del d
+        torch.cuda.empty_cache()
+    return out
+
+
+# ------------------------------------------------------- reference arm --
+
+def run_reference(args, rank, world):
+    """The CPU oracle as the reference arm, on the same workload, metric and
+    unit: chained rows=1 bf16 blocks, timed on the host cores. Steps are capped
+    so the run ends within a few minutes; the metric is a rate."""
+    if rank != 0:
+        return None
+    cap_s = args.ref_seconds
+    import numpy as np
+    import torch
+
+    import oracle
+    from hyper_connection_rank_gb300 import inputs as I
+    oracle.build()
+    codes = lambda t: t.contiguous().view(torch.int16).numpy().view(np.uint16)
+    ws = [{k: codes(v) for k, v in I.make_weights(C, H, R, "bf16", seed=0, block=i).items()} for i in range(2)]
+    act = {k: codes(v) for k, v in I.make_activations(1, C, H, "bf16", seed=0, block=0, prologue=True).items()}
+
+    def one(i, act):
+        w = ws[i % 2]
+        pre, post, sout = oracle.lowrank_mix(act["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
+                                             act["prev_out"], act["prev_gate"], num_branches=C,
+                                             dtype=oracle.DT_BF16, nthreads=1, **QWEN)
+        return {"streams": sout, "prev_out": pre, "prev_gate": post}
+
+    for i in range(args.warmup):
+        act = one(i, act)
+    n, t0 = 0, time.perf_counter()
+    while n < args.steps:
+        act = one(n, act)
+        n += 1
+        if time.perf_counter() - t0 > cap_s:
+            break
+    el = time.perf_counter() - t0
+    v = n / el
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 2), "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "steps_timed": n, "warmup": args.warmup, "ms_per_step": 1000 * el / n,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": WORKLOAD.replace("graph replay", "CPU oracle, 2 weight sets"),
+                                            "rows": 1, "C": C, "H": H, "R": R},
+            "cpu_baseline": {"value": round(v, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{n} chained decode blocks on 1 host thread ({el:.1f} s)"},
+            "e2e": {"value": round(v, 2), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=96 * 2000)
+    ap.add_argument("--warmup", type=int, default=96)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3000)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(local_rank)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

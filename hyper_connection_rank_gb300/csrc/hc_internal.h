@@ -1,0 +1,91 @@
+// Host-side interfaces between the C ABI layer and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstddef>
+#include <cstdint>
+#include <utility>
+
+#include "hc_lowrank_mix.h"
+
+namespace hc {
+
+// One validated call, as the launchers see it.
+struct Problem {
+  const void *streams, *norm_scale, *down_w, *up_w, *inject_w, *prev_out, *prev_gate;
+  int64_t rows;
+  int C, H, R;
+  float eps, rho, alpha, gate_div, gate_mul;
+  uint32_t flags;
+  hc_dtype_t dt;
+  void *pre_output, *post_gate, *streams_out;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaStream_t stream;
+  int num_sms;
+};
+
+inline size_t dtype_size(hc_dtype_t dt) { return dt == HC_F32 ? 4 : 2; }
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// General CUDA-core path: any shape, any rows, any T, any alignment.
+size_t general_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+cudaError_t launch_general(const Problem& p);
+
+// Decode path: rows <= 8, split-K weight streaming (hc_decode.cu).
+bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
+cudaError_t launch_decode(const Problem& p);
+// Diagnostic counter of bounded device waits that gave up.
+unsigned int read_wait_timeouts(bool reset);
+
+// Opt a kernel in to `bytes` of dynamic shared memory on the current device.
+// The attribute is set once per kernel and device and remembered, so later
+// calls (including calls made while a stream is being captured into a graph)
+// issue no further runtime calls.
+template <auto Kernel>
+cudaError_t ensure_smem(size_t bytes) {
+  static std::atomic<size_t> granted[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e == cudaSuccess && dev >= 0 && dev < 64) {
+    size_t cur = granted[dev].load(std::memory_order_acquire);
+    while (cur < bytes && !granted[dev].compare_exchange_weak(cur, bytes)) {
+    }
+  }
+  return e;
+}
+
+// Launch with programmatic stream serialisation (PDL) and an optional
+// cluster shape along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[n].val.programmaticStreamSerializationAllowed = 1;
+  ++n;
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+}  // namespace hc

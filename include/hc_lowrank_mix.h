@@ -1,0 +1,136 @@
+/* hc_lowrank_mix.h -- C ABI of the GB300 (sm_103a) hyper-connection low-rank mix block.
+ *
+ * The operation is the fused block defined in ONNX Runtime pull request #33384,
+ * "com.microsoft.HyperConnectionLowRankMix", sections "Schema summary" and
+ * "Numerics contract":
+ *
+ *   S          = streams + prev_post_gate * prev_block_output   (optional prologue; else S = streams)
+ *   hn         = S / sqrt(mean_h(S^2) + epsilon) * norm_scale    (per branch c, over its H features)
+ *   down       = hn @ down_weight                                (K = C*H, N = R)
+ *   d          = ScaledSiLU(down, silu_alpha) = down * sigmoid(silu_alpha * down)
+ *   g          = sigmoid(d @ up_weight)                          (per stream and feature)
+ *   pre_output = reduction_scale * sum_c (hn * g)                (shape (..., H))
+ *   post_gate  = sigmoid((hn @ inject_weight) / gate_div) * gate_mul   (shape (..., C))
+ *   streams_out = S
+ *
+ * Numerics: products and reductions accumulate in fp32; every step is rounded
+ * once to T at S, hn, down, Z (= silu_alpha*down), SG (= sigmoid(Z)), hidden
+ * (= down*SG = d), up, g, pre_output, inject, post_gate; the sigmoid is
+ * 1/(1+expf(-x)) in fp32 with an IEEE divide. Accumulation order is fixed for a
+ * given shape and path: results are bitwise deterministic, and a row's bits do
+ * not depend on the number of rows within one path (see hc_lowrank_mix_path).
+ *
+ * Memory: every tensor argument is a DEVICE pointer to contiguous row-major
+ * data of element type T (all tensors share T). The caller owns all memory;
+ * the library never allocates, never synchronises the host, and keeps no
+ * state between calls, so a call can be captured in a CUDA graph.
+ */
+#ifndef HC_LOWRANK_MIX_H
+#define HC_LOWRANK_MIX_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is struct CUstream_st* */
+
+typedef enum {
+  HC_OK = 0,
+  HC_ERR_INVALID_ARG = 1, /* null required pointer, bad size, half a prologue, aliasing outputs */
+  HC_ERR_UNSUPPORTED = 2, /* device is not sm_103, or a size beyond the library's limits */
+  HC_ERR_WORKSPACE = 3,   /* workspace missing, too small, or not 256-byte aligned */
+  HC_ERR_CUDA = 4         /* a CUDA runtime call failed (hc_last_error() has the text) */
+} hc_status_t;
+
+/* Element type T of every tensor ("T = float / float16 / bfloat16"). */
+typedef enum { HC_F32 = 0, HC_F16 = 1, HC_BF16 = 2 } hc_dtype_t;
+
+/* Operator attributes ("Schema summary", Attributes). num_branches is the C
+ * argument of the calls below. */
+typedef struct {
+  float epsilon;          /* default 1e-5 */
+  float reduction_scale;  /* default 1 */
+  float silu_alpha;       /* default 1 */
+  float gate_div;         /* default 1 */
+  float gate_mul;         /* default 1 */
+  uint32_t flags;         /* HC_FLAG_* below */
+} hc_attrs_t;
+
+/* The weights (norm_scale, down, up, inject) are not written by any kernel
+ * still running on the stream when this call is made. The first kernel may
+ * then stream its weights before waiting for the previous kernel (programmatic
+ * dependent launch). Without the flag it waits first. */
+#define HC_FLAG_WEIGHTS_STATIC 1u
+/* Run the general CUDA-core path even where a specialised path applies
+ * (for cross-path checks). */
+#define HC_FLAG_FORCE_GENERAL 2u
+
+/* Path selected for a call (hc_lowrank_mix_path). */
+#define HC_PATH_NONE 0    /* rows == 0: nothing is launched */
+#define HC_PATH_DECODE 1  /* rows <= 8: split-K weight-streaming GEMV pair */
+#define HC_PATH_PREFILL 2 /* many rows, fp16/bf16: tcgen05 tensor-core contractions */
+#define HC_PATH_GENERAL 3 /* any shape, any rows, any T: CUDA-core kernels */
+
+/* Attribute defaults of the schema: {1e-5, 1, 1, 1, 1, flags 0}. */
+hc_attrs_t hc_attrs_default(void);
+
+/* Which path hc_lowrank_mix takes for these sizes on the current device, given
+ * that every pointer is 16-byte aligned (misaligned pointers select
+ * HC_PATH_GENERAL). Returns a HC_PATH_* value, or -1 for invalid sizes. */
+int hc_lowrank_mix_path(int64_t rows, int C, int H, int R, hc_dtype_t dt, uint32_t flags);
+
+/* Bytes of device workspace hc_lowrank_mix needs for these sizes and flags
+ * (0 if none). The workspace is scratch: it may hold anything on entry and
+ * holds nothing useful on return. */
+size_t hc_lowrank_mix_workspace_size(int64_t rows, int C, int H, int R, hc_dtype_t dt, uint32_t flags);
+
+/* Enqueue one block on `stream` (NULL = the legacy default stream).
+ *
+ * Inputs (device, type T, contiguous):
+ *   streams     (rows, C*H): element (b, c, h) at b*C*H + c*H + h
+ *   norm_scale  (C*H)
+ *   down_w      (C*H, R) row-major [K, N]
+ *   up_w        (R, C*H) row-major [K, N]
+ *   inject_w    (C*H, C) row-major [K, N]
+ *   prev_out    (rows, H)  prev_block_output, or NULL
+ *   prev_gate   (rows, C)  prev_post_gate, or NULL; both prologue inputs or neither
+ * Outputs (device, type T, contiguous, written in full):
+ *   pre_output  (rows, H)
+ *   post_gate   (rows, C)
+ *   streams_out (rows, C*H) or NULL: S after the prologue (a copy of streams without one)
+ * Outputs must not overlap each other, any input, or the workspace.
+ * attrs: NULL means hc_attrs_default().
+ * workspace: device buffer of at least hc_lowrank_mix_workspace_size(...) bytes,
+ *   256-byte aligned; may be NULL when that size is 0.
+ * rows == 0 returns HC_OK and launches nothing; row pointers may then be NULL.
+ *
+ * Errors are detected on the host before anything is launched and returned as a
+ * status; hc_last_error() gives a description (per calling thread). Faults
+ * during execution surface on the stream, as for any CUDA kernel. */
+hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const void* down_w,
+                           const void* up_w, const void* inject_w, const void* prev_out,
+                           const void* prev_gate, int64_t rows, int C, int H, int R,
+                           const hc_attrs_t* attrs, hc_dtype_t dt, void* pre_output,
+                           void* post_gate, void* streams_out, void* workspace,
+                           size_t workspace_bytes, struct CUstream_st* stream);
+
+/* Static name of a status code. */
+const char* hc_status_string(hc_status_t status);
+
+/* Description of the last error returned on the calling thread ("" if none). */
+const char* hc_last_error(void);
+
+/* Diagnostic: how many bounded device-side waits (on asynchronous copies) gave
+ * up since the last reset; 0 in normal operation. A wait gives up after about
+ * one second, writes NaN into the affected outputs and lets the kernel finish.
+ * Synchronises with the current device; reset != 0 clears the count. */
+unsigned int hc_debug_wait_timeouts(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_LOWRANK_MIX_H */

@@ -1,0 +1,262 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the CPU oracle.
+
+Cases follow the operator's own test grid (ONNX Runtime PR #33384, "Testing"):
+the real shape 4 x 2560, rank 320, for fp32 / fp16 / bf16, several row
+counts, with and without the prologue; small and irregular shapes; default and
+non-default attributes; two chained blocks; bitwise row independence;
+streams_out pass-through; zero rows; CUDA-graph capture and replay bitwise
+equal to eager. Plus determinism over repeated runs, guard bands around every
+output, and misaligned pointers.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _parity import KEYS, compare, run_gpu, run_oracle
+from _util import TORCH_DT, to_codes
+from hyper_connection_rank_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+DEFAULT_ATTRS = dict(epsilon=1e-5, reduction_scale=1.0, silu_alpha=1.0, gate_div=1.0, gate_mul=1.0)
+ODD_ATTRS = dict(epsilon=0.5, reduction_scale=1.5, silu_alpha=2.0, gate_div=0.7, gate_mul=3.0)
+
+
+@pytest.fixture(scope="module")
+def hc():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__
+    __graft_entry__.build()
+    import hyper_connection_rank_gb300 as m
+    m.debug_wait_timeouts(reset=True)
+    yield m
+    assert m.debug_wait_timeouts() == 0, "a bounded device wait gave up"
+
+
+def check(hc, rows, C, H, R, dt, prologue=True, attrs=I.QWEN_ATTRS, seed=0, flags=0, expect_path=None):
+    d = I.make_block(rows, C, H, R, dt, seed=seed, prologue=prologue)
+    if expect_path is not None:
+        assert hc.path(rows, C, H, R, TORCH_DT[dt], flags) == expect_path
+    gpu = run_gpu(hc, d, C, attrs, flags=flags)
+    ref = run_oracle(d, C, dt, attrs)
+    return compare(gpu, ref, dt, C, H, R, attrs)
+
+
+# ------------------------------------------------------------ tiny config --
+
+@pytest.mark.parametrize("flags", [0, 2], ids=["auto", "general"])
+def test_tiny_fp32_block(hc, flags):
+    """rows=2, C=4, H=64, R=16, fp32, no prologue, Qwen attributes, seed 0."""
+    check(hc, 2, 4, 64, 16, "f32", prologue=False, flags=flags)
+
+
+# --------------------------------------------------- real shape, decode rows --
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("prologue", [True, False])
+def test_real_shape_decode(hc, dt, rows, prologue):
+    st = check(hc, rows, 4, 2560, 320, dt, prologue=prologue, expect_path=hc.HC_PATH_DECODE)
+    print(dt, rows, prologue, st)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("rows", [1, 8])
+def test_second_prefill_shape_decode_rows(hc, dt, rows):
+    """C=8, H=1280, R=320 (the second prefill shape) at decode row counts."""
+    check(hc, rows, 8, 1280, 320, dt, expect_path=hc.HC_PATH_DECODE)
+
+
+@pytest.mark.parametrize("attrs", [DEFAULT_ATTRS, ODD_ATTRS], ids=["default", "odd"])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_attributes(hc, attrs, dt):
+    check(hc, 3, 4, 2560, 320, dt, attrs=attrs)
+
+
+# ------------------------------------------------- small / irregular shapes --
+
+SHAPES = [(1, 64, 8), (2, 32, 16), (3, 40, 24), (4, 64, 16), (8, 32, 32), (4, 4096, 512), (1, 4096, 64),
+          (2, 1000, 33), (8, 128, 512)]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "C%d_H%d_R%d" % s)
+@pytest.mark.parametrize("rows", [1, 7])
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_small_and_irregular_shapes(hc, shape, rows, dt):
+    C, H, R = shape
+    check(hc, rows, C, H, R, dt, seed=3)
+
+
+# ---------------------------------------------- general path, more rows --
+
+@pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows", [9, 16, 128])
+def test_real_shape_more_rows(hc, dt, rows):
+    check(hc, rows, 4, 2560, 320, dt)
+
+
+@pytest.mark.parametrize("dt,C,H", [("bf16", 4, 2560), ("f16", 8, 1280)])
+def test_prefill_size_sampled_rows(hc, dt, C, H):
+    """rows = 8192 at the prefill shapes; the oracle checks a sample of rows
+    spread over the batch (first, last, and every 509th)."""
+    rows, R = 8192, 320
+    d = I.make_block(rows, C, H, R, dt, seed=0, prologue=True)
+    gpre, gpost, gsout = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    idx = np.unique(np.concatenate([np.arange(0, rows, 509), [1, rows - 2, rows - 1]]))
+    ref = run_oracle(d, C, dt, I.QWEN_ATTRS, rows_idx=torch.from_numpy(idx))
+    compare((gpre[idx], gpost[idx], gsout[idx]), ref, dt, C, H, R, I.QWEN_ATTRS)
+
+
+# ----------------------------------------------------------- invariants --
+
+@pytest.mark.parametrize("rows,flags", [(8, 0), (8, 2), (40, 2)], ids=["decode", "general", "general40"])
+def test_row_independence_bitwise(hc, rows, flags):
+    """A row gives the same bits at any batch size, within one path."""
+    C, H, R = 4, 2560, 320
+    d = I.make_block(rows, C, H, R, "bf16", seed=5, prologue=True)
+    full = run_gpu(hc, d, C, I.QWEN_ATTRS, flags=flags)
+    for j in (0, rows // 2, rows - 1):
+        one = {k: (v[j:j + 1] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+        r = run_gpu(hc, one, C, I.QWEN_ATTRS, flags=flags)
+        for a, b in zip(full, r):
+            assert np.array_equal(a[j:j + 1], b)
+
+
+@pytest.mark.parametrize("rows,flags", [(1, 0), (8, 0), (16, 0), (4, 2)])
+def test_deterministic_over_20_runs(hc, rows, flags):
+    d = I.make_block(rows, 4, 2560, 320, "bf16", seed=6, prologue=True)
+    first = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=flags)
+    for _ in range(19):
+        again = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=flags)
+        for a, b in zip(first, again):
+            assert np.array_equal(a, b)
+
+
+def test_streams_out_passthrough_and_optional(hc):
+    d = I.make_block(3, 4, 2560, 320, "bf16", seed=7, prologue=False)
+    pre, post, sout = run_gpu(hc, d, 4, I.QWEN_ATTRS)
+    assert np.array_equal(sout, to_codes(d["streams"]))
+    pre2, post2, none = run_gpu(hc, d, 4, I.QWEN_ATTRS, want_streams_out=False)
+    assert none is None and np.array_equal(pre, pre2) and np.array_equal(post, post2)
+
+
+def test_zero_up_and_inject_weights(hc):
+    d = I.make_block(2, 4, 2560, 320, "bf16", seed=8, prologue=True)
+    d["up_w"] = torch.zeros_like(d["up_w"])
+    d["inject_w"] = torch.zeros_like(d["inject_w"])
+    gpu = run_gpu(hc, d, 4, I.QWEN_ATTRS)
+    compare(gpu, run_oracle(d, 4, "bf16", I.QWEN_ATTRS), "bf16", 4, 2560, 320, I.QWEN_ATTRS)
+    post = torch.from_numpy(gpu[1].view(np.int16)).view(torch.bfloat16).float()
+    assert torch.all(post == 1.0)  # gate_mul / 2
+
+
+def test_zero_rows(hc):
+    d = I.make_block(0, 4, 2560, 320, "bf16", seed=0, prologue=True)
+    pre, post, sout = run_gpu(hc, d, 4, I.QWEN_ATTRS)
+    assert pre.shape == (0, 2560) and post.shape == (0, 4) and sout.shape == (0, 10240)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f32"])
+def test_two_chained_blocks(hc, dt):
+    """Block 2's prologue takes block 1's pre_output and post_gate, and its
+    streams are block 1's streams_out; each side runs its own chain."""
+    C, H, R, rows = 4, 2560, 320, 2
+    d1 = I.make_block(rows, C, H, R, dt, seed=9, block=0, prologue=True)
+    w2 = I.make_weights(C, H, R, dt, seed=9, block=1)
+    g1 = run_gpu(hc, d1, C, I.QWEN_ATTRS)
+    o1 = run_oracle(d1, C, dt, I.QWEN_ATTRS)
+    compare(g1, o1, dt, C, H, R, I.QWEN_ATTRS)
+    from _util import from_codes
+    g2 = run_gpu(hc, dict(w2, streams=from_codes(g1[2], dt), prev_out=from_codes(g1[0], dt),
+                          prev_gate=from_codes(g1[1], dt)), C, I.QWEN_ATTRS)
+    o2 = run_oracle(dict(w2, streams=from_codes(o1[2], dt), prev_out=from_codes(o1[0], dt),
+                         prev_gate=from_codes(o1[1], dt)), C, dt, I.QWEN_ATTRS)
+    compare(g2, o2, dt, C, H, R, I.QWEN_ATTRS, check_streams_out=False)
+
+
+@pytest.mark.parametrize("rows", [1, 8, 64])
+def test_cuda_graph_replay_bitwise_equal_to_eager(hc, rows):
+    C, H, R = 4, 2560, 320
+    d = I.make_block(rows, C, H, R, "bf16", seed=10, prologue=True)
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    eager = hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, **I.QWEN_ATTRS)
+    torch.cuda.synchronize()
+    pre = torch.empty_like(eager[0]); post = torch.empty_like(eager[1]); sout = torch.empty_like(eager[2])
+    ws = torch.empty(hc.workspace_size(rows, C, H, R, torch.bfloat16), dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(graph, stream=s):
+            hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, out=(pre, post, sout), workspace=ws,
+                           **I.QWEN_ATTRS)
+    for _ in range(3):
+        pre.zero_(); post.zero_(); sout.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(eager, (pre, post, sout)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_guard_bands_untouched(hc):
+    """Outputs and workspace sit inside larger buffers filled with a sentinel;
+    the bytes around them must survive the call (stands in for memcheck)."""
+    C, H, R = 4, 2560, 320
+    for rows, flags in ((3, 0), (3, 2), (20, 0)):
+        d = I.make_block(rows, C, H, R, "bf16", seed=11, prologue=True)
+        g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+        pad = 4096
+
+        def guarded(n):
+            buf = torch.full((n + 2 * pad,), 0x5A5A, dtype=torch.int16, device="cuda")
+            return buf, buf[pad:pad + n].view(torch.bfloat16)
+
+        bp, pre = guarded(rows * H)
+        bq, post = guarded(rows * C)
+        bs, sout = guarded(rows * C * H)
+        nws = hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)
+        wbuf = torch.full((nws + 2 * 8192,), 0xA5, dtype=torch.uint8, device="cuda")
+        ws = wbuf[8192:8192 + nws]
+        hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, out=(pre.view(rows, H), post.view(rows, C),
+                                                                    sout.view(rows, C * H)),
+                       workspace=ws, flags=flags, **I.QWEN_ATTRS)
+        torch.cuda.synchronize()
+        for buf, n in ((bp, rows * H), (bq, rows * C), (bs, rows * C * H)):
+            assert torch.all(buf[:pad] == 0x5A5A) and torch.all(buf[pad + n:] == 0x5A5A)
+        assert torch.all(wbuf[:8192] == 0xA5) and torch.all(wbuf[8192 + nws:] == 0xA5)
+
+
+def test_misaligned_pointers_take_general_path(hc):
+    C, H, R, rows = 4, 256, 32, 3
+    d = I.make_block(rows, C, H, R, "bf16", seed=12, prologue=True)
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    big = torch.empty(rows * C * H + 1, dtype=torch.bfloat16, device="cuda")
+    st = big[1:].view(rows, C * H)          # 2-byte offset: not 16-byte aligned
+    st.copy_(g["streams"])
+    out = hc.lowrank_mix(st, *[g[k] for k in KEYS[1:]], num_branches=C, **I.QWEN_ATTRS)
+    torch.cuda.synchronize()
+    ref = run_oracle(d, C, "bf16", I.QWEN_ATTRS)
+    compare(tuple(to_codes(t) for t in out), ref, "bf16", C, H, R, I.QWEN_ATTRS)
+
+
+def test_workspace_errors(hc):
+    C, H, R, rows = 4, 2560, 320, 2
+    d = I.make_block(rows, C, H, R, "bf16", seed=0, prologue=True)
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    need = hc.workspace_size(rows, C, H, R, torch.bfloat16)
+    assert need > 0
+    small = torch.empty(need // 2, dtype=torch.uint8, device="cuda")
+    with pytest.raises(hc.HcError) as e:
+        hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, workspace=small, **I.QWEN_ATTRS)
+    assert e.value.status == 3
+
+
+def test_cross_path_agreement(hc):
+    """Decode and general paths accumulate in different orders; both meet the
+    oracle tolerance, and they agree with each other on most elements."""
+    d = I.make_block(4, 4, 2560, 320, "bf16", seed=13, prologue=True)
+    a = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=0)
+    b = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=2)
+    assert np.array_equal(a[2], b[2])
+    assert (a[0] == b[0]).mean() > 0.8
