@@ -146,9 +146,11 @@ def run_ours(args, rank, world, local_rank):
         if dist:
             tdist.barrier()
 
-    rows = 1
+    rows = args.rows
     flags = hc.HC_FLAG_WEIGHTS_STATIC
     assert hc.path(rows, C, H, R, torch.bfloat16, flags) == hc.HC_PATH_DECODE
+    if args.profile_case:
+        return profile_case(args, hc, I, dev, rows, flags)
     weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(NSETS)]
     bufs = [I.make_activations(rows, C, H, "bf16", seed=0, block=0, prologue=True, device=dev)]
     bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
@@ -233,6 +235,24 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         result["sweep"] = sweep(hc, I, dev, pk)
     return result
+
+
+def profile_case(args, hc, I, dev, rows, flags):
+    """Small case for profiler captures: the same decode block, 4 weight sets
+    (53 MB), eager launches through the public API; prints a JSON line but is
+    not a benchmark result (profiler captures flush caches per pass anyway)."""
+    import torch
+    weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(4)]
+    bufs = [I.make_activations(rows, C, H, "bf16", seed=0, block=0, prologue=True, device=dev)]
+    bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
+    ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
+    for i in range(args.warmup + args.steps):
+        src, dst, w = bufs[i % 2], bufs[(i + 1) % 2], weights[i % 4]
+        hc.lowrank_mix(src["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], src["prev_out"],
+                       src["prev_gate"], num_branches=C, flags=flags,
+                       out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
+    torch.cuda.synchronize()
+    return {"profile_case": f"decode rows={rows} bf16, 4 weight sets, {args.warmup}+{args.steps} eager blocks"}
 
 
 def e2e_measure(args, hc, I, weights, dev, flags):
@@ -464,6 +484,9 @@ def main():
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--rows", type=int, default=1, help="decode rows per block (1..8)")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="small eager case for profiler captures (not a benchmark result)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

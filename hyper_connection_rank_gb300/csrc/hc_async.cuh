@@ -67,4 +67,29 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (bypasses L1), grouped by
+// commit_group / wait_group.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// v(0) + v(1) + ... + v(n-1) added in that order, with the loads behind v
+// issued eight at a time so their latencies overlap.
+template <class F>
+__device__ __forceinline__ float ordered_sum(int n, F v) {
+  float t = 0.0f;
+  int p = 0;
+  for (; p + 8 <= n; p += 8) {
+    float x[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = v(p + j);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t += x[j];
+  }
+  for (; p < n; ++p) t += v(p);
+  return t;
+}
+
 }  // namespace hc

@@ -20,8 +20,8 @@
 //       GEMV for down and inject, and reduces the CL partial vectors of its
 //       cluster through DSMEM in rank order into one fp32 partial per cluster.
 //   dec_up (grid = (H/HS)*C CTAs, clusters of C CTAs, one per branch)
-//     - bulk-copies its up_weight tile (R rows x HS columns of branch c) and
-//       loads S for its tile before griddepcontrol.wait;
+//     - copies its up_weight tile (R rows x HS columns of branch c) with
+//       16-byte cp.async and loads S for its tile before griddepcontrol.wait;
 //     - reduces the down partials (each rank 1/C of the R columns, partials
 //       added in cluster order), applies ScaledSiLU, and broadcasts d to the
 //       cluster through DSMEM;
@@ -48,12 +48,12 @@ namespace {
 
 constexpr int kUpThreads = 256;
 
-// 16-byte vector of T from shared memory, widened to fp32.
+// 16-byte vectors of T, widened to fp32 and narrowed back (values that are
+// already representable in T pass through exactly).
 template <typename T> struct Vec;
 template <> struct Vec<__nv_bfloat16> {
   static constexpr int N = 8;
-  static __device__ __forceinline__ void load(const unsigned char* p, float* out) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+  static __device__ __forceinline__ void unpack(const uint4& u, float* out) {
     const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -62,11 +62,17 @@ template <> struct Vec<__nv_bfloat16> {
       out[2 * i + 1] = f.y;
     }
   }
+  static __device__ __forceinline__ uint4 pack(const float* in) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+    return u;
+  }
 };
 template <> struct Vec<__half> {
   static constexpr int N = 8;
-  static __device__ __forceinline__ void load(const unsigned char* p, float* out) {
-    const uint4 u = *reinterpret_cast<const uint4*>(p);
+  static __device__ __forceinline__ void unpack(const uint4& u, float* out) {
     const __half2* h = reinterpret_cast<const __half2*>(&u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -75,48 +81,75 @@ template <> struct Vec<__half> {
       out[2 * i + 1] = f.y;
     }
   }
+  static __device__ __forceinline__ uint4 pack(const float* in) {
+    uint4 u;
+    __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
+    return u;
+  }
 };
 template <> struct Vec<float> {
   static constexpr int N = 4;
-  static __device__ __forceinline__ void load(const unsigned char* p, float* out) {
-    const float4 f = *reinterpret_cast<const float4*>(p);
-    out[0] = f.x; out[1] = f.y; out[2] = f.z; out[3] = f.w;
+  static __device__ __forceinline__ void unpack(const uint4& u, float* out) {
+    out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+    out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* in) {
+    return make_uint4(__float_as_uint(in[0]), __float_as_uint(in[1]), __float_as_uint(in[2]), __float_as_uint(in[3]));
   }
 };
 
+template <typename T> __device__ __forceinline__ uint4 ld16(const T* p) { return *reinterpret_cast<const uint4*>(p); }
+template <typename T> __device__ __forceinline__ void st16(T* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
+
+// Cluster barrier halves. Every CTA of a cluster arrives early (relaxed: no
+// memory ordering) and waits just before its first store into a peer's
+// shared memory, which guarantees that every peer has started.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Full cluster barrier: stores into peers' shared memory made before it are
+// visible to them after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __host__ __device__ inline uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Shared-memory layout of dec_down (byte offsets), for MB rows.
 struct DownSmem {
-  uint32_t bar, wd, wi, hn, wsum, ssq, inv, red, part, total;
+  uint32_t bar, wd, wi, ns, hn, wsum, inv, red, recv, total;
 };
 __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int CL, int nwarps, int es) {
+  const int ncr = ceil_div(R + C, CL);
   DownSmem L;
   L.bar = 0;
   L.wd = 16;
   L.wi = a16(L.wd + KS * R * es);
-  L.hn = a16(L.wi + KS * C * es);
+  L.ns = a16(L.wi + KS * C * es);
+  L.hn = a16(L.ns + KS * 4);
   L.wsum = a16(L.hn + MB * KS * 4);
-  L.ssq = a16(L.wsum + nwarps * MB * 4);
-  L.inv = a16(L.ssq + CL * MB * 4);
+  L.inv = a16(L.wsum + nwarps * MB * 4);
   L.red = a16(L.inv + MB * 4);
-  L.part = a16(L.red + MB * R * 4);
-  L.total = a16(L.part + MB * (R + C) * 4);
+  L.recv = a16(L.red + MB * R * 4);
+  L.total = a16(L.recv + CL * MB * ncr * 4);
   return L;
 }
 
 // Shared-memory layout of dec_up (byte offsets), for MB rows.
 struct UpSmem {
-  uint32_t bar, wu, s, ns, d, red, mix, total;
+  uint32_t wu, d, hn, ns, red, mix, total;
 };
 __host__ __device__ inline UpSmem up_smem(int MB, int HS, int R, int nwarps, int es) {
   UpSmem L;
-  L.bar = 0;
-  L.wu = 16;
-  L.s = a16(L.wu + R * HS * es);
-  L.ns = a16(L.s + MB * HS * 4);
-  L.d = a16(L.ns + HS * 4);
-  L.red = a16(L.d + MB * R * 4);
+  L.wu = 0;
+  L.d = a16(L.wu + R * HS * es);
+  L.hn = a16(L.d + MB * R * 4);
+  L.ns = a16(L.hn + MB * HS * 4);
+  L.red = a16(L.ns + HS * 4);
   L.mix = a16(L.red + nwarps * MB * HS * 4);
   L.total = a16(L.mix + MB * HS * 4);
   return L;
@@ -127,8 +160,8 @@ struct DownArgs {
   const T *streams, *prev_out, *prev_gate, *ns, *wd, *wi;
   T* sout;
   float* inv_ws;   // (B, C)
-  float* part_ws;  // (NCLU, B, R + C)
-  int B, C, H, R, KS, CL, KQ;
+  float* part_ws;  // (NCLU, B, NCP)
+  int B, C, H, R, KS, CL, KQ, NCP;
   float eps;
   int weights_static;
 };
@@ -139,19 +172,9 @@ struct UpArgs {
   const float* inv_ws;
   const float* part_ws;
   T *pre, *post;
-  int B, C, H, R, HS, NP;
+  int B, C, H, R, HS, NP, NCP, split_d;
   Attrs at;
 };
-
-// S(b, c, h) of the prologue, recomputed wherever it is needed (same bits).
-template <typename T>
-__device__ __forceinline__ float s_at(const T* streams, const T* prev_out, const T* prev_gate, int b, int c,
-                                      int h, int C, int H) {
-  const int64_t CH = static_cast<int64_t>(C) * H;
-  float v = ldf(streams + b * CH + static_cast<int64_t>(c) * H + h);
-  if (prev_out != nullptr) v = prologue_s<T>(v, ldf(prev_gate + b * C + c), ldf(prev_out + static_cast<int64_t>(b) * H + h));
-  return v;
-}
 
 template <typename T, int MB>
 __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
@@ -160,16 +183,17 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   constexpr int es = sizeof(T);
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
   const int B = a.B, C = a.C, H = a.H, R = a.R, KS = a.KS, CL = a.CL, NC = R + C;
+  const int ncr = ceil_div(NC, CL);
   const DownSmem L = down_smem(MB, KS, R, C, CL, nwarps, es);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   unsigned char* wd_s = smem + L.wd;
   const T* wi_s = reinterpret_cast<const T*>(smem + L.wi);
+  float* ns_s = reinterpret_cast<float*>(smem + L.ns);
   float* hn_s = reinterpret_cast<float*>(smem + L.hn);
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
-  float* ssq_s = reinterpret_cast<float*>(smem + L.ssq);
   float* inv_s = reinterpret_cast<float*>(smem + L.inv);
   float* red_s = reinterpret_cast<float*>(smem + L.red);
-  float* part_s = reinterpret_cast<float*>(smem + L.part);
+  float* recv_s = reinterpret_cast<float*>(smem + L.recv);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -180,35 +204,68 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   const uint32_t wbytes = static_cast<uint32_t>(KS * R * es), ibytes = static_cast<uint32_t>(KS * C * es);
   const bool pro = a.prev_out != nullptr;
 
+  cluster_arrive_relaxed();
   if (tid == 0) {
     mbar_init(bar, 1);
     fence_mbar_init();
   }
   __syncthreads();
-  if (a.weights_static && tid == 0) {
-    mbar_arrive_expect_tx(bar, wbytes + ibytes);
-    bulk_g2s(wd_s, a.wd + static_cast<int64_t>(k0) * R, wbytes, bar);
-    bulk_g2s(smem + L.wi, a.wi + static_cast<int64_t>(k0) * C, ibytes, bar);
-  }
+  auto issue_weights = [&]() {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(bar, wbytes + ibytes);
+      bulk_g2s(wd_s, a.wd + static_cast<int64_t>(k0) * R, wbytes, bar);
+      bulk_g2s(smem + L.wi, a.wi + static_cast<int64_t>(k0) * C, ibytes, bar);
+    }
+    for (int i = tid; i < KS / VEC; i += nthr) {
+      float f[VEC];
+      Vec<T>::unpack(ld16(a.ns + k0 + i * VEC), f);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) ns_s[i * VEC + j] = f[j];
+    }
+  };
+  if (a.weights_static) issue_weights();
   pdl_wait();
-  if (!a.weights_static && tid == 0) {
-    mbar_arrive_expect_tx(bar, wbytes + ibytes);
-    bulk_g2s(wd_s, a.wd + static_cast<int64_t>(k0) * R, wbytes, bar);
-    bulk_g2s(smem + L.wi, a.wi + static_cast<int64_t>(k0) * C, ibytes, bar);
-  }
+  if (!a.weights_static) issue_weights();
   pdl_trigger();
 
-  // ---- branch RMS: this rank sums S^2 over its 1/CL of branch c ----
-  const int hc = H / CL, hlo = rank * hc;
+  // ---- one pass over branch c of every row: S, its sum of squares, the
+  // slice's S (kept in shared memory) and streams_out for the slice ----
+  const int NVr = H / VEC;
   float ss[MB];
 #pragma unroll
   for (int b = 0; b < MB; ++b) ss[b] = 0.0f;
-  for (int h = hlo + tid; h < hlo + hc; h += nthr) {
+  for (int v = tid; v < NVr; v += nthr) {
+    uint4 sv[MB], pv[MB];
+    float gt[MB];
 #pragma unroll
     for (int b = 0; b < MB; ++b)
       if (b < B) {
-        const float v = s_at(a.streams, a.prev_out, a.prev_gate, b, c, h, C, H);
-        ss[b] = fmaf(v, v, ss[b]);
+        sv[b] = ld16(a.streams + b * CH + static_cast<int64_t>(c) * H + v * VEC);
+        if (pro) {
+          pv[b] = ld16(a.prev_out + static_cast<int64_t>(b) * H + v * VEC);
+          gt[b] = ldf(a.prev_gate + b * C + c);
+        }
+      }
+    const int kk = v * VEC - hk0;
+    const bool mine = kk >= 0 && kk < KS;
+#pragma unroll
+    for (int b = 0; b < MB; ++b)
+      if (b < B) {
+        float sf[VEC];
+        Vec<T>::unpack(sv[b], sf);
+        if (pro) {
+          float pf[VEC];
+          Vec<T>::unpack(pv[b], pf);
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) sf[j] = prologue_s<T>(sf[j], gt[b], pf[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) ss[b] = fmaf(sf[j], sf[j], ss[b]);
+        if (mine) {
+#pragma unroll
+          for (int j = 0; j < VEC; ++j) hn_s[b * KS + kk + j] = sf[j];
+          if (a.sout != nullptr) st16(a.sout + b * CH + k0 + kk, pro ? Vec<T>::pack(sf) : sv[b]);
+        }
       }
   }
 #pragma unroll
@@ -220,28 +277,14 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   if (tid < B) {
     float t = 0.0f;
     for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + tid];
-    for (int pr = 0; pr < CL; ++pr) cluster.map_shared_rank(ssq_s, pr)[rank * MB + tid] = t;
-  }
-  cluster.sync();
-  if (tid < B) {
-    float t = 0.0f;
-    for (int r = 0; r < CL; ++r) t += ssq_s[r * MB + tid];
     const float iv = inv_rms(t, H, a.eps);
     inv_s[tid] = iv;
     if (hk0 == 0) a.inv_ws[tid * C + c] = iv;
   }
   __syncthreads();
-
-  // ---- hn for this slice; streams_out for this slice ----
   for (int i = tid; i < B * KS; i += nthr) {
     const int b = i / KS, kk = i - b * KS;
-    const float v = s_at(a.streams, a.prev_out, a.prev_gate, b, c, hk0 + kk, C, H);
-    if (a.sout != nullptr) {
-      const int64_t o = b * CH + k0 + kk;
-      if (pro) stf(a.sout + o, v);
-      else a.sout[o] = a.streams[o];
-    }
-    hn_s[b * KS + kk] = norm_hn<T>(v, inv_s[b], ldf(a.ns + k0 + kk));
+    hn_s[i] = norm_hn<T>(hn_s[i], inv_s[b], ns_s[kk]);
   }
   __syncthreads();
   const bool ok = mbar_wait(bar, 0, &g_wait_timeouts);
@@ -262,7 +305,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
     const unsigned char* wrow = wd_s + static_cast<size_t>(kg * rpk) * R * es + v * 16;
     for (int i = 0; i < rpk; ++i) {
       float w[VEC];
-      Vec<T>::load(wrow + static_cast<size_t>(i) * R * es, w);
+      Vec<T>::unpack(*reinterpret_cast<const uint4*>(wrow + static_cast<size_t>(i) * R * es), w);
       const int kk = kg * rpk + i;
 #pragma unroll
       for (int b = 0; b < MB; ++b)
@@ -289,6 +332,15 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
         for (int j = 0; j < VEC; ++j) red_s[b * R + v * VEC + j] = acc[b][j];
   }
   __syncthreads();
+
+  // ---- push this CTA's partial sums to the cluster rank that owns each
+  // column (rank r owns columns [r*ncr, (r+1)*ncr) of [down | inject]) ----
+  cluster_wait();
+  auto push = [&](int b, int col, float val) {
+    const int ow = col / ncr;
+    cluster.map_shared_rank(recv_s, ow)[(rank * MB + b) * ncr + (col - ow * ncr)] = val;
+  };
+  const float qnan = __int_as_float(0x7fc00000);
   if (kq == 0 && leader) {
 #pragma unroll
     for (int b = 0; b < MB; ++b)
@@ -297,29 +349,52 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
         for (int j = 0; j < VEC; ++j) {
           float t = acc[b][j];
           if (a.KQ == 2) t += red_s[b * R + v * VEC + j];
-          part_s[b * NC + v * VEC + j] = ok ? t : __int_as_float(0x7fc00000);
+          push(b, v * VEC + j, ok ? t : qnan);
         }
   }
-  // inject: KS-term dot products, one thread per (row, branch)
-  for (int i = tid; i < B * C; i += nthr) {
-    const int b = i / C, cc = i - b * C;
+  // inject: one warp per (row, branch), lanes over k, butterfly sum
+  for (int p = warp; p < B * C; p += nwarps) {
+    const int b = p / C, cc = p - b * C;
     float t = 0.0f;
     if (ok)
-      for (int kk = 0; kk < KS; ++kk) t = fmaf(hn_s[b * KS + kk], ldf(wi_s + kk * C + cc), t);
-    part_s[b * NC + R + cc] = ok ? t : __int_as_float(0x7fc00000);
+      for (int kk = lane; kk < KS; kk += 32) t = fmaf(hn_s[b * KS + kk], ldf(wi_s + kk * C + cc), t);
+    t = warp_sum(t);
+    if (lane == 0) push(b, R + cc, ok ? t : qnan);
   }
-  cluster.sync();
+  cluster_sync_all();
 
-  // ---- cluster reduction of the partial vectors, in rank order ----
-  const int ncr = (NC + CL - 1) / CL, clo = rank * ncr, chi = min(NC, clo + ncr), nmine = max(0, chi - clo);
+  // ---- reduce the received partials of the owned columns in rank order ----
+  const int clo = rank * ncr, nmine = max(0, min(NC, clo + ncr) - clo);
   const int cluster_id = slice / CL;
   for (int i = tid; i < B * nmine; i += nthr) {
-    const int b = i / nmine, col = clo + (i - b * nmine);
+    const int b = i / nmine, lc = i - b * nmine;
+    float x[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) x[r] = r < CL ? recv_s[(r * MB + b) * ncr + lc] : 0.0f;
     float t = 0.0f;
-    for (int r = 0; r < CL; ++r) t += cluster.map_shared_rank(part_s, r)[b * NC + col];
-    a.part_ws[(static_cast<int64_t>(cluster_id) * B + b) * NC + col] = t;
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+      if (r < CL) t += x[r];
+    a.part_ws[(static_cast<int64_t>(cluster_id) * B + b) * a.NCP + clo + lc] = t;
   }
-  cluster.sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+// Ordered sum over p of the float4 at src + p * stride (in float4 units),
+// loads issued 16 at a time.
+__device__ __forceinline__ float4 ordered_sum4(const float4* src, int64_t stride, int n) {
+  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+  int p = 0;
+  for (; p < n; p += 16) {
+    float4 x[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = p + j < n ? src[(p + j) * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+      if (p + j < n) {
+        t.x += x[j].x; t.y += x[j].y; t.z += x[j].z; t.w += x[j].w;
+      }
+  }
+  return t;
 }
 
 template <typename T, int MB>
@@ -328,13 +403,12 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   constexpr int VEC = Vec<T>::N;
   constexpr int es = sizeof(T);
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
-  const int B = a.B, C = a.C, H = a.H, R = a.R, HS = a.HS, NC = R + C;
+  const int B = a.B, C = a.C, H = a.H, R = a.R, HS = a.HS;
   const UpSmem L = up_smem(MB, HS, R, nwarps, es);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   unsigned char* wu_s = smem + L.wu;
-  float* s_s = reinterpret_cast<float*>(smem + L.s);
-  float* ns_s = reinterpret_cast<float*>(smem + L.ns);
   float* d_s = reinterpret_cast<float*>(smem + L.d);
+  float* hn_s = reinterpret_cast<float*>(smem + L.hn);
+  float* ns_s = reinterpret_cast<float*>(smem + L.ns);
   float* red_s = reinterpret_cast<float*>(smem + L.red);
   float* mix_s = reinterpret_cast<float*>(smem + L.mix);
 
@@ -345,52 +419,101 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   const int64_t CH = static_cast<int64_t>(C) * H;
   const int64_t col0 = static_cast<int64_t>(c) * H + h0;
   const uint32_t rowbytes = static_cast<uint32_t>(HS * es);
+  const bool pro = a.prev_out != nullptr;
 
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
+  cluster_arrive_relaxed();
   // The up weights and the block inputs are never written by the preceding
   // dec_down, which triggers its dependents only after its own wait: reading
-  // them before griddepcontrol.wait is safe.
-  if (tid == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(R) * rowbytes);
-  __syncwarp();
-  if (warp == 0)
-    for (int r = lane; r < R; r += 32) bulk_g2s(wu_s + static_cast<size_t>(r) * rowbytes, a.wu + r * CH + col0, rowbytes, bar);
-  for (int i = tid; i < B * HS; i += nthr) {
-    const int b = i / HS, h = i - b * HS;
-    s_s[i] = s_at(a.streams, a.prev_out, a.prev_gate, b, c, h0 + h, C, H);
+  // them before griddepcontrol.wait is safe. The tile is R rows of HS
+  // contiguous elements: 16-byte cp.async chunks, consecutive threads on
+  // consecutive chunks of a row.
+  {
+    const int cpr = static_cast<int>(rowbytes / 16);
+    const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wu + col0);
+    for (int i = tid; i < R * cpr; i += nthr) {
+      const int r = i / cpr, qd = i - r * cpr;
+      cp_async16(wu_s + static_cast<size_t>(r) * rowbytes + qd * 16, gsrc + (static_cast<int64_t>(r) * CH) * es + qd * 16);
+    }
+    cp_async_commit();
   }
-  for (int i = tid; i < HS; i += nthr) ns_s[i] = ldf(a.ns + col0 + i);
+  const int nvh = HS / VEC;
+  for (int i = tid; i < B * nvh; i += nthr) {
+    const int b = i / nvh, qv = i - b * nvh;
+    float sf[VEC];
+    Vec<T>::unpack(ld16(a.streams + b * CH + col0 + qv * VEC), sf);
+    if (pro) {
+      float pf[VEC];
+      Vec<T>::unpack(ld16(a.prev_out + static_cast<int64_t>(b) * H + h0 + qv * VEC), pf);
+      const float gt = ldf(a.prev_gate + b * C + c);
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) sf[j] = prologue_s<T>(sf[j], gt, pf[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) hn_s[b * HS + qv * VEC + j] = sf[j];
+  }
+  for (int i = tid; i < nvh; i += nthr) {
+    float f[VEC];
+    Vec<T>::unpack(ld16(a.ns + col0 + i * VEC), f);
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) ns_s[i * VEC + j] = f[j];
+  }
   pdl_wait();
   pdl_trigger();
-  __syncthreads();
+  cluster_wait();
+  __syncthreads();  // S (in hn_s) and ns_s were written by other threads above
+  float inv_r[MB];
+#pragma unroll
+  for (int b = 0; b < MB; ++b) inv_r[b] = b < B ? a.inv_ws[b * C + c] : 0.0f;
 
-  // ---- down partials -> d for this rank's share of R, broadcast to the cluster
-  const int rc = (R + C - 1) / C, rlo = c * rc, rhi = min(R, rlo + rc), nr = max(0, rhi - rlo);
-  for (int i = tid; i < B * nr; i += nthr) {
-    const int b = i / nr, r = rlo + (i - b * nr);
-    float t = 0.0f;
-    for (int p = 0; p < a.NP; ++p) t += a.part_ws[(static_cast<int64_t>(p) * B + b) * NC + r];
-    const float d = scaled_silu<T>(rT<T>(t), a.at.alpha);
-    for (int pr = 0; pr < C; ++pr) cluster.map_shared_rank(d_s, pr)[b * R + r] = d;
+  // ---- d = ScaledSiLU(rT(sum of the down partials)), in float4 column
+  // groups; at most 2 rows every CTA reduces all R columns itself, above
+  // that each cluster rank reduces 1/C of them and broadcasts over DSMEM ----
+  const int NR4 = R / 4, NP = a.NP;
+  const int64_t pstride4 = static_cast<int64_t>(B) * a.NCP / 4;
+  int g_lo = 0, g_hi = NR4;
+  if (a.split_d) {
+    const int per = ceil_div(NR4, C);
+    g_lo = min(NR4, c * per);
+    g_hi = min(NR4, g_lo + per);
+  }
+  const int ng = g_hi - g_lo;
+  for (int i = tid; i < B * ng; i += nthr) {
+    const int b = i / ng, g = g_lo + (i - b * ng);
+    const float4* src = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP) + g;
+    const float4 t = ordered_sum4(src, pstride4, NP);
+    float dv[4] = {scaled_silu<T>(rT<T>(t.x), a.at.alpha), scaled_silu<T>(rT<T>(t.y), a.at.alpha),
+                   scaled_silu<T>(rT<T>(t.z), a.at.alpha), scaled_silu<T>(rT<T>(t.w), a.at.alpha)};
+    if (a.split_d) {
+      for (int pr = 0; pr < C; ++pr) {
+        float* dst = cluster.map_shared_rank(d_s, pr) + b * R + g * 4;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) dst[j] = dv[j];
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) d_s[b * R + g * 4 + j] = dv[j];
+    }
   }
   if (q == 0 && c == 0) {
     for (int i = tid; i < B * C; i += nthr) {
       const int b = i / C, cc = i - b * C;
-      float t = 0.0f;
-      for (int p = 0; p < a.NP; ++p) t += a.part_ws[(static_cast<int64_t>(p) * B + b) * NC + R + cc];
+      const float* src = a.part_ws + static_cast<int64_t>(b) * a.NCP + R + cc;
+      const int64_t pstride = static_cast<int64_t>(B) * a.NCP;
+      const float t = ordered_sum(NP, [&](int p) { return src[p * pstride]; });
       stf(a.post + b * C + cc, post_gate_of<T>(rT<T>(t), a.at.gate_div, a.at.gate_mul));
     }
   }
-  // hn of this tile, in place
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
-    s_s[i] = norm_hn<T>(s_s[i], a.inv_ws[b * C + c], ns_s[h]);
+    float iv = inv_r[0];
+#pragma unroll
+    for (int bb = 1; bb < MB; ++bb)
+      if (bb == b) iv = inv_r[bb];
+    hn_s[i] = norm_hn<T>(hn_s[i], iv, ns_s[h]);
   }
-  cluster.sync();
-  const bool ok = mbar_wait(bar, 0, &g_wait_timeouts);
+  if (a.split_d) cluster_sync_all();
+  cp_async_wait_all();
+  __syncthreads();
 
   // ---- up GEMV: NVh lanes cover one row of the tile, rows strided over groups
   const int NVh = HS / VEC;
@@ -401,18 +524,16 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   for (int b = 0; b < MB; ++b)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[b][j] = 0.0f;
-  if (ok) {
-    for (int r = rg; r < R; r += RG) {
-      float w[VEC];
-      Vec<T>::load(wu_s + static_cast<size_t>(r) * rowbytes + lv * 16, w);
+  for (int r = rg; r < R; r += RG) {
+    float w[VEC];
+    Vec<T>::unpack(*reinterpret_cast<const uint4*>(wu_s + static_cast<size_t>(r) * rowbytes + lv * 16), w);
 #pragma unroll
-      for (int b = 0; b < MB; ++b)
-        if (b < B) {
-          const float dv = d_s[b * R + r];
+    for (int b = 0; b < MB; ++b)
+      if (b < B) {
+        const float dv = d_s[b * R + r];
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[b][j] = fmaf(dv, w[j], acc[b][j]);
-        }
-    }
+        for (int j = 0; j < VEC; ++j) acc[b][j] = fmaf(dv, w[j], acc[b][j]);
+      }
   }
   for (int o = NVh; o < 32; o <<= 1)
 #pragma unroll
@@ -428,23 +549,30 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   }
   __syncthreads();
 
-  // ---- up -> g -> hn*g, sent to the rank that finalises that feature
+  // ---- up -> g -> hn*g; the pre-mix sums the products over c = 0..C-1 on
+  // the rank that finalises the feature (rank j owns features [j*HSc, ...)) ----
   const int HSc = HS / C;
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
     float u = 0.0f;
     for (int w = 0; w < nwarps; ++w) u += red_s[(w * MB + b) * HS + h];
     const float g = rT<T>(sigmoid_acc(rT<T>(u)));
-    const float prod = ok ? __fmul_rn(s_s[i], g) : __int_as_float(0x7fc00000);
-    const int j = h / HSc, hl = h - j * HSc;
-    cluster.map_shared_rank(mix_s, j)[(c * MB + b) * HSc + hl] = prod;
+    const float prod = __fmul_rn(hn_s[i], g);
+    if (C == 1) {
+      stf(a.pre + static_cast<int64_t>(b) * H + h0 + h, __fmul_rn(a.at.rho, __fadd_rn(0.0f, prod)));
+    } else {
+      const int j = h / HSc, hl = h - j * HSc;
+      cluster.map_shared_rank(mix_s, j)[(c * MB + b) * HSc + hl] = prod;
+    }
   }
-  cluster.sync();
-  for (int i = tid; i < B * HSc; i += nthr) {
-    const int b = i / HSc, hl = i - b * HSc;
-    float acc2 = 0.0f;
-    for (int cc = 0; cc < C; ++cc) acc2 = __fadd_rn(acc2, mix_s[(cc * MB + b) * HSc + hl]);
-    stf(a.pre + static_cast<int64_t>(b) * H + h0 + c * HSc + hl, __fmul_rn(a.at.rho, acc2));
+  if (C > 1) {
+    cluster_sync_all();
+    for (int i = tid; i < B * HSc; i += nthr) {
+      const int b = i / HSc, hl = i - b * HSc;
+      float acc2 = 0.0f;
+      for (int cc = 0; cc < C; ++cc) acc2 = __fadd_rn(acc2, mix_s[(cc * MB + b) * HSc + hl]);
+      stf(a.pre + static_cast<int64_t>(b) * H + h0 + c * HSc + hl, __fmul_rn(a.at.rho, acc2));
+    }
   }
 }
 
@@ -486,6 +614,10 @@ DecodeCfg decode_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_s
   return g;
 }
 
+// Row stride of the fp32 partials: R + C padded to a multiple of 4 floats so
+// the R down columns can be read as float4.
+inline int partial_stride(int R, int C) { return (R + C + 3) / 4 * 4; }
+
 struct DecLayout {
   size_t inv, part, total;
 };
@@ -493,7 +625,7 @@ DecLayout dec_layout(int64_t rows, int C, int R, const DecodeCfg& g) {
   DecLayout L;
   L.inv = 0;
   L.part = align_up(static_cast<size_t>(rows) * C * 4, 256);
-  L.total = align_up(L.part + static_cast<size_t>(g.NCLU) * rows * (R + C) * 4, 256);
+  L.total = align_up(L.part + static_cast<size_t>(g.NCLU) * rows * partial_stride(R, C) * 4, 256);
   return L;
 }
 
@@ -517,6 +649,7 @@ cudaError_t run_decode_mb(const Problem& p, const DecodeCfg& g) {
   da.part_ws = part_ws;
   da.B = static_cast<int>(p.rows);
   da.C = p.C; da.H = p.H; da.R = p.R; da.KS = g.KS; da.CL = g.CL; da.KQ = g.KQ;
+  da.NCP = partial_stride(p.R, p.C);
   da.eps = p.eps;
   da.weights_static = (p.flags & HC_FLAG_WEIGHTS_STATIC) ? 1 : 0;
   const size_t dsm = down_smem(MB, g.KS, p.R, p.C, g.CL, g.down_threads / 32, es).total;
@@ -536,6 +669,8 @@ cudaError_t run_decode_mb(const Problem& p, const DecodeCfg& g) {
   ua.pre = static_cast<T*>(p.pre_output);
   ua.post = static_cast<T*>(p.post_gate);
   ua.B = da.B; ua.C = p.C; ua.H = p.H; ua.R = p.R; ua.HS = g.HS; ua.NP = g.NCLU;
+  ua.NCP = da.NCP;
+  ua.split_d = (p.rows > 2 && p.C > 1) ? 1 : 0;
   ua.at = Attrs{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
   const size_t usm = up_smem(MB, g.HS, p.R, g.up_threads / 32, es).total;
   e = ensure_smem<dec_up<T, MB>>(usm);
