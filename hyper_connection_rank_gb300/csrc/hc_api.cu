@@ -81,6 +81,10 @@ size_t workspace_for(int path, int64_t rows, int C, int H, int R, hc_dtype_t dt,
 
 }  // namespace
 
+namespace hc {
+hc_status_t set_error(hc_status_t s, const char* msg) { return fail(s, "%s", msg); }
+}  // namespace hc
+
 extern "C" {
 
 hc_attrs_t hc_attrs_default(void) {

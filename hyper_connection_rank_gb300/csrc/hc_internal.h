@@ -38,6 +38,9 @@ cudaError_t launch_general(const Problem& p);
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode(const Problem& p);
+// Record `msg` as this thread's hc_last_error() text and return `s`.
+hc_status_t set_error(hc_status_t s, const char* msg);
+
 // Diagnostic counter of bounded device waits that gave up.
 unsigned int read_wait_timeouts(bool reset);
 

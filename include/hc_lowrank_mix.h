@@ -117,6 +117,33 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
                            void* post_gate, void* streams_out, void* workspace,
                            size_t workspace_bytes, struct CUstream_st* stream);
 
+/* hc_lowrank_mix for callers that cannot allocate device memory.
+ *
+ * The page that defines the block has no counterpart to this entry point.
+ * Some callers cannot provide a workspace: a host whose memory pool owns the
+ * whole GPU and refuses later allocations, a plug-in interface that passes
+ * tensors and a stream but no allocator, or code running inside a strict
+ * (global-mode) stream capture, where an allocation would break the capture.
+ * This variant runs the decode path with its scratch in a fixed 1 MiB device
+ * array inside the library (per GPU, held until the process exits) and
+ * allocates nothing.
+ *
+ * Arguments and outputs are those of hc_lowrank_mix without the workspace.
+ * Only decode-path problems fit (rows <= 8, C in {1,2,4,8}, H % 16 == 0,
+ * R % 8 == 0, R <= 512, every pointer 16-byte aligned, partial sums within
+ * 1 MiB; the 4 x 2560, rank-320 block uses about 210 KB at 8 rows); anything
+ * else returns HC_ERR_UNSUPPORTED with the reason in hc_last_error().
+ * All calls share the one array and it keeps the last call's contents (the
+ * kernels need no cleared scratch); calls whose kernels may run at the same
+ * time on one GPU, such as calls on two unordered streams, race on it.
+ * The first call on each device looks up the array's address (with that
+ * device current); make that call before capturing a stream that uses it. */
+hc_status_t hc_lowrank_mix_decode_noalloc(const void* streams, const void* norm_scale, const void* down_w,
+                                          const void* up_w, const void* inject_w, const void* prev_out,
+                                          const void* prev_gate, int64_t rows, int C, int H, int R,
+                                          const hc_attrs_t* attrs, hc_dtype_t dt, void* pre_output,
+                                          void* post_gate, void* streams_out, struct CUstream_st* stream);
+
 /* Static name of a status code. */
 const char* hc_status_string(hc_status_t status);
 
