@@ -31,6 +31,7 @@
 //
 // All reductions have a fixed order that depends on the shape only, so the
 // results are deterministic and a row's bits do not depend on the row count.
+#include <algorithm>
 #include <cooperative_groups.h>
 
 #include "hc_async.cuh"
@@ -123,8 +124,12 @@ __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; 
 struct DownSmem {
   uint32_t bar, wd, wi, ns, hn, wsum, inv, red, recv, total;
 };
+// Columns of [down | inject] owned by each cluster rank in the partial-sum
+// reduction: a multiple of 4 so a float4 group never straddles two owners.
+__host__ __device__ inline int owner_cols(int R, int C, int CL) { return ceil_div(ceil_div(R + C, CL), 4) * 4; }
+
 __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int CL, int nwarps, int es) {
-  const int ncr = ceil_div(R + C, CL);
+  const int ncr = owner_cols(R, C, CL);
   DownSmem L;
   L.bar = 0;
   L.wd = 16;
@@ -141,12 +146,14 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
 
 // Shared-memory layout of dec_up (byte offsets), for MB rows.
 struct UpSmem {
-  uint32_t wu, d, hn, ns, red, mix, total;
+  uint32_t wu, csum, d, hn, ns, red, mix, total;
 };
-__host__ __device__ inline UpSmem up_smem(int MB, int HS, int R, int nwarps, int es) {
+// csum_bytes: the chunk sums of the partial reduction (see dec_up).
+__host__ __device__ inline UpSmem up_smem(int MB, int HS, int R, int nwarps, int es, int csum_bytes) {
   UpSmem L;
   L.wu = 0;
-  L.d = a16(L.wu + R * HS * es);
+  L.csum = a16(L.wu + R * HS * es);
+  L.d = a16(L.csum + csum_bytes);
   L.hn = a16(L.d + MB * R * 4);
   L.ns = a16(L.hn + MB * HS * 4);
   L.red = a16(L.ns + HS * 4);
@@ -172,7 +179,7 @@ struct UpArgs {
   const float* inv_ws;
   const float* part_ws;
   T *pre, *post;
-  int B, C, H, R, HS, NP, NCP, split_d;
+  int B, C, H, R, HS, NP, NCP, split_d, nch, csum_bytes;
   Attrs at;
 };
 
@@ -183,7 +190,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   constexpr int es = sizeof(T);
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
   const int B = a.B, C = a.C, H = a.H, R = a.R, KS = a.KS, CL = a.CL, NC = R + C;
-  const int ncr = ceil_div(NC, CL);
+  const int ncr = owner_cols(R, C, CL);
   const DownSmem L = down_smem(MB, KS, R, C, CL, nwarps, es);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   unsigned char* wd_s = smem + L.wd;
@@ -303,16 +310,24 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
     for (int j = 0; j < VEC; ++j) acc[b][j] = 0.0f;
   if (ok && kq < a.KQ && v < NV) {
     const unsigned char* wrow = wd_s + static_cast<size_t>(kg * rpk) * R * es + v * 16;
-    for (int i = 0; i < rpk; ++i) {
-      float w[VEC];
-      Vec<T>::unpack(*reinterpret_cast<const uint4*>(wrow + static_cast<size_t>(i) * R * es), w);
-      const int kk = kg * rpk + i;
+    for (int i0 = 0; i0 < rpk; i0 += 8) {
+      uint4 wv[8];
 #pragma unroll
-      for (int b = 0; b < MB; ++b)
-        if (b < B) {
-          const float hv = hn_s[b * KS + kk];
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u < rpk) wv[u] = *reinterpret_cast<const uint4*>(wrow + static_cast<size_t>(i0 + u) * R * es);
 #pragma unroll
-          for (int j = 0; j < VEC; ++j) acc[b][j] = fmaf(hv, w[j], acc[b][j]);
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u < rpk) {
+          float w[VEC];
+          Vec<T>::unpack(wv[u], w);
+          const int kk = kg * rpk + i0 + u;
+#pragma unroll
+          for (int b = 0; b < MB; ++b)
+            if (b < B) {
+              const float hv = hn_s[b * KS + kk];
+#pragma unroll
+              for (int j = 0; j < VEC; ++j) acc[b][j] = fmaf(hv, w[j], acc[b][j]);
+            }
         }
     }
   }
@@ -346,10 +361,17 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
     for (int b = 0; b < MB; ++b)
       if (b < B)
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) {
-          float t = acc[b][j];
-          if (a.KQ == 2) t += red_s[b * R + v * VEC + j];
-          push(b, v * VEC + j, ok ? t : qnan);
+        for (int j0 = 0; j0 < VEC; j0 += 4) {
+          float t[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            t[j] = acc[b][j0 + j];
+            if (a.KQ == 2) t[j] += red_s[b * R + v * VEC + j0 + j];
+            if (!ok) t[j] = qnan;
+          }
+          const int col = v * VEC + j0, ow = col / ncr;
+          float* dst = cluster.map_shared_rank(recv_s, ow) + (rank * MB + b) * ncr + (col - ow * ncr);
+          *reinterpret_cast<float4*>(dst) = make_float4(t[0], t[1], t[2], t[3]);
         }
   }
   // inject: one warp per (row, branch), lanes over k, butterfly sum
@@ -379,24 +401,6 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   }
 }
 
-// Ordered sum over p of the float4 at src + p * stride (in float4 units),
-// loads issued 16 at a time.
-__device__ __forceinline__ float4 ordered_sum4(const float4* src, int64_t stride, int n) {
-  float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-  int p = 0;
-  for (; p < n; p += 16) {
-    float4 x[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) x[j] = p + j < n ? src[(p + j) * stride] : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int j = 0; j < 16; ++j)
-      if (p + j < n) {
-        t.x += x[j].x; t.y += x[j].y; t.z += x[j].z; t.w += x[j].w;
-      }
-  }
-  return t;
-}
-
 template <typename T, int MB>
 __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -404,8 +408,9 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   constexpr int es = sizeof(T);
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
   const int B = a.B, C = a.C, H = a.H, R = a.R, HS = a.HS;
-  const UpSmem L = up_smem(MB, HS, R, nwarps, es);
+  const UpSmem L = up_smem(MB, HS, R, nwarps, es, a.csum_bytes);
   unsigned char* wu_s = smem + L.wu;
+  float4* csum_s = reinterpret_cast<float4*>(smem + L.csum);
   float* d_s = reinterpret_cast<float*>(smem + L.d);
   float* hn_s = reinterpret_cast<float*>(smem + L.hn);
   float* ns_s = reinterpret_cast<float*>(smem + L.ns);
@@ -477,29 +482,92 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
     g_hi = min(NR4, g_lo + per);
   }
   const int ng = g_hi - g_lo;
-  for (int i = tid; i < B * ng; i += nthr) {
-    const int b = i / ng, g = g_lo + (i - b * ng);
-    const float4* src = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP) + g;
-    const float4 t = ordered_sum4(src, pstride4, NP);
-    float dv[4] = {scaled_silu<T>(rT<T>(t.x), a.at.alpha), scaled_silu<T>(rT<T>(t.y), a.at.alpha),
-                   scaled_silu<T>(rT<T>(t.z), a.at.alpha), scaled_silu<T>(rT<T>(t.w), a.at.alpha)};
-    if (a.split_d) {
-      for (int pr = 0; pr < C; ++pr) {
-        float* dst = cluster.map_shared_rank(d_s, pr) + b * R + g * 4;
+  // Work unit = (float4 column group of one row, chunk of the partials): the
+  // NP partials are cut into nch chunks; each unit sums its chunk in partial
+  // order, loads issued together (two units per thread in flight), and the
+  // chunk sums are then added in chunk order. CTA (0, 0) also reduces the
+  // inject columns (scalars) the same way for post_gate.
+  const int nch = a.nch, cs = ceil_div(NP, nch);
+  const bool do_post = (q == 0 && c == 0);
+  const int n_items = B * ng, n_units = n_items * nch;
+  const int n_post_units = do_post ? B * C * nch : 0;
+  float* psum_s = reinterpret_cast<float*>(csum_s + static_cast<size_t>(n_items) * nch);
+  for (int u0 = tid; u0 < n_units + n_post_units; u0 += 2 * nthr) {
+    float4 x[2][8];
+    float y[2][8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) dst[j] = dv[j];
+    for (int k = 0; k < 2; ++k) {
+      const int u = u0 + k * nthr;
+      const bool post_unit = u >= n_units;
+      const int uu = post_unit ? u - n_units : u;
+      const int item = uu / nch, ch = uu - item * nch;
+      const int p_lo = ch * cs;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bool live = u < n_units + n_post_units && j < cs && p_lo + j < NP;
+        x[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        y[k][j] = 0.0f;
+        if (live && !post_unit) {
+          const int b = item / ng, g = g_lo + (item - b * ng);
+          x[k][j] = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP)[g + (p_lo + j) * pstride4];
+        } else if (live) {
+          const int b = item / C, cc = item - b * C;
+          y[k][j] = a.part_ws[(static_cast<int64_t>(p_lo + j) * B + b) * a.NCP + R + cc];
+        }
       }
-    } else {
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) d_s[b * R + g * 4 + j] = dv[j];
+    for (int k = 0; k < 2; ++k) {
+      const int u = u0 + k * nthr;
+      if (u >= n_units + n_post_units) continue;
+      const bool post_unit = u >= n_units;
+      const int uu = post_unit ? u - n_units : u;
+      const int item = uu / nch, ch = uu - item * nch;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      float ty = 0.0f;
+      const int cnt = min(cs, NP - ch * cs);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < cnt) {
+          t.x += x[k][j].x; t.y += x[k][j].y; t.z += x[k][j].z; t.w += x[k][j].w;
+          ty += y[k][j];
+        }
+      for (int p = 8; p < cnt; ++p) {
+        if (!post_unit) {  // chunks longer than 8: remaining loads one by one
+          const int b = item / ng, g = g_lo + (item - b * ng);
+          const float4 z = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP)[g + (ch * cs + p) * pstride4];
+          t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
+        } else {
+          const int b = item / C, cc = item - b * C;
+          ty += a.part_ws[(static_cast<int64_t>(ch * cs + p) * B + b) * a.NCP + R + cc];
+        }
+      }
+      if (post_unit) psum_s[ch * (B * C) + item] = ty;
+      else csum_s[ch * n_items + item] = t;
     }
   }
-  if (q == 0 && c == 0) {
+  __syncthreads();
+  for (int i = tid; i < n_items; i += nthr) {
+    const int b = i / ng, g = g_lo + (i - b * ng);
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int ch = 0; ch < nch; ++ch) {
+      const float4 z = csum_s[ch * n_items + i];
+      t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
+    }
+    const float4 dv = make_float4(scaled_silu<T>(rT<T>(t.x), a.at.alpha), scaled_silu<T>(rT<T>(t.y), a.at.alpha),
+                                  scaled_silu<T>(rT<T>(t.z), a.at.alpha), scaled_silu<T>(rT<T>(t.w), a.at.alpha));
+    if (a.split_d) {
+      for (int pr = 0; pr < C; ++pr)
+        *reinterpret_cast<float4*>(cluster.map_shared_rank(d_s, pr) + b * R + g * 4) = dv;
+    } else {
+      *reinterpret_cast<float4*>(d_s + b * R + g * 4) = dv;
+    }
+  }
+  if (do_post) {
     for (int i = tid; i < B * C; i += nthr) {
+      float t = 0.0f;
+      for (int ch = 0; ch < nch; ++ch) t += psum_s[ch * (B * C) + i];
       const int b = i / C, cc = i - b * C;
-      const float* src = a.part_ws + static_cast<int64_t>(b) * a.NCP + R + cc;
-      const int64_t pstride = static_cast<int64_t>(B) * a.NCP;
-      const float t = ordered_sum(NP, [&](int p) { return src[p * pstride]; });
       stf(a.post + b * C + cc, post_gate_of<T>(rT<T>(t), a.at.gate_div, a.at.gate_mul));
     }
   }
@@ -671,8 +739,14 @@ cudaError_t run_decode_mb(const Problem& p, const DecodeCfg& g) {
   ua.B = da.B; ua.C = p.C; ua.H = p.H; ua.R = p.R; ua.HS = g.HS; ua.NP = g.NCLU;
   ua.NCP = da.NCP;
   ua.split_d = (p.rows > 2 && p.C > 1) ? 1 : 0;
+  {
+    const int NR4 = p.R / 4;
+    const int ng = ua.split_d ? (NR4 + p.C - 1) / p.C : NR4;
+    ua.nch = std::max(1, std::min(8, (g.NCLU + 7) / 8));
+    ua.csum_bytes = static_cast<int>(ua.nch * (static_cast<size_t>(p.rows) * ng * 16 + static_cast<size_t>(p.rows) * p.C * 4));
+  }
   ua.at = Attrs{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
-  const size_t usm = up_smem(MB, g.HS, p.R, g.up_threads / 32, es).total;
+  const size_t usm = up_smem(MB, g.HS, p.R, g.up_threads / 32, es, ua.csum_bytes).total;
   e = ensure_smem<dec_up<T, MB>>(usm);
   if (e != cudaSuccess) return e;
   return launch_pdl(dec_up<T, MB>, dim3((p.H / g.HS) * p.C), dim3(g.up_threads), usm, p.stream,
