@@ -482,7 +482,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
     g_hi = min(NR4, g_lo + per);
   }
   const int ng = g_hi - g_lo;
-  // Work unit = (float4 column group of one row, chunk of the partials): the
+  // Work unit = (chunk of the partials, float4 column group of one row): the
   // NP partials are cut into nch chunks; each unit sums its chunk in partial
   // order, loads issued together (two units per thread in flight), and the
   // chunk sums are then added in chunk order. CTA (0, 0) also reduces the
@@ -500,7 +500,8 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
       const int u = u0 + k * nthr;
       const bool post_unit = u >= n_units;
       const int uu = post_unit ? u - n_units : u;
-      const int item = uu / nch, ch = uu - item * nch;
+      const int nk = post_unit ? B * C : n_items;  // consecutive units: consecutive items of one chunk
+      const int ch = uu / nk, item = uu - ch * nk;
       const int p_lo = ch * cs;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -522,7 +523,8 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
       if (u >= n_units + n_post_units) continue;
       const bool post_unit = u >= n_units;
       const int uu = post_unit ? u - n_units : u;
-      const int item = uu / nch, ch = uu - item * nch;
+      const int nk = post_unit ? B * C : n_items;  // consecutive units: consecutive items of one chunk
+      const int ch = uu / nk, item = uu - ch * nk;
       float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
       float ty = 0.0f;
       const int cnt = min(cs, NP - ch * cs);
