@@ -67,6 +67,7 @@ int select_path(int64_t rows, int C, int H, int R, hc_dtype_t dt, uint32_t flags
   if (flags & HC_FLAG_FORCE_GENERAL) return HC_PATH_GENERAL;
   if (!all_aligned) return HC_PATH_GENERAL;
   if (hc::decode_supported(rows, C, H, R, dt)) return HC_PATH_DECODE;
+  if (hc::prefill_supported(rows, C, H, R, dt)) return HC_PATH_PREFILL;
   (void)num_sms;
   return HC_PATH_GENERAL;
 }
@@ -74,6 +75,7 @@ int select_path(int64_t rows, int C, int H, int R, hc_dtype_t dt, uint32_t flags
 size_t workspace_for(int path, int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   switch (path) {
     case HC_PATH_DECODE: return hc::decode_workspace(rows, C, H, R, dt, num_sms);
+    case HC_PATH_PREFILL: return hc::prefill_workspace(rows, C, H, R, dt);
     case HC_PATH_GENERAL: return hc::general_workspace(rows, C, H, R, dt);
     default: return 0;
   }
@@ -202,6 +204,7 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
   cudaError_t e = cudaSuccess;
   switch (path) {
     case HC_PATH_DECODE: e = hc::launch_decode(p); break;
+    case HC_PATH_PREFILL: e = hc::launch_prefill(p); break;
     default: e = hc::launch_general(p); break;
   }
   if (e != cudaSuccess) return fail(HC_ERR_CUDA, "launch failed: %s", cudaGetErrorString(e));
@@ -210,6 +213,8 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
 
 /* Diagnostic: number of bounded device waits that gave up since the last
  * reset (normally 0). Synchronises with the device. */
-unsigned int hc_debug_wait_timeouts(int reset) { return hc::read_wait_timeouts(reset != 0); }
+unsigned int hc_debug_wait_timeouts(int reset) {
+  return hc::read_wait_timeouts(reset != 0) + hc::read_pf_wait_timeouts(reset != 0);
+}
 
 }  // extern "C"

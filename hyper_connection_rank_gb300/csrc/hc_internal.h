@@ -38,6 +38,12 @@ cudaError_t launch_general(const Problem& p);
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode(const Problem& p);
+// Prefill path: many rows, fp16/bf16, tcgen05 contractions (hc_prefill.cu).
+bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+size_t prefill_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+cudaError_t launch_prefill(const Problem& p);
+unsigned int read_pf_wait_timeouts(bool reset);
+
 // Record `msg` as this thread's hc_last_error() text and return `s`.
 hc_status_t set_error(hc_status_t s, const char* msg);
 

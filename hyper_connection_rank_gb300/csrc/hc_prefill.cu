@@ -1,0 +1,564 @@
+// Prefill path of the low-rank mix block (many rows, fp16/bf16): the down and
+// up projections are dense contractions on the 5th-generation tensor cores
+// (tcgen05, fp32 accumulators in tensor memory), fed by TMA tensor copies.
+//
+//   pf_norm  (one CTA per row, CUDA cores): prologue S -> streams_out, the
+//            branch RMS statistic, hn -> workspace, inject = hn @ W_i and
+//            post_gate (C x C*H work per row is too small for a tensor tile).
+//   pf_down  (tcgen05): partial[ks] = hn[:, K_ks] @ W_d[K_ks, :] for the
+//            branch-sized K slices ks, 128-row tiles, W_d read in place as an
+//            MN-major operand. Fixed split by branch, so a row's sums never
+//            depend on the number of rows.
+//   pf_mid   : down = rT(sum of the partials in slice order), ScaledSiLU -> d.
+//   pf_up    (tcgen05): up = d @ W_u for a tile of 128 rows x (C branches x
+//            64 features); the epilogue reads the accumulators from tensor
+//            memory and computes g = rT(sigmoid(rT(up))), hn * g, the pre-mix
+//            over the branches in order and pre_output, all in registers.
+//
+// Pipelines: one TMA thread, one MMA thread, four epilogue warps; stage
+// hand-off through mbarriers (all waits bounded, see hc_async.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "hc_async.cuh"
+#include "hc_common.cuh"
+#include "hc_internal.h"
+#include "hc_tc.cuh"
+
+namespace hc {
+
+// Count of bounded waits in this file's kernels that gave up (diagnostic).
+__device__ unsigned int g_pf_wait_timeouts = 0;
+
+namespace {
+
+constexpr int kBM = 128;            // tile rows = tensor-memory lanes
+constexpr int kBK = 64;             // K per stage = one 128-byte swizzle row
+constexpr int kBoxBytes = 64 * 64 * 2;
+constexpr int kATileBytes = kBM * kBK * 2;
+constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
+constexpr int kNormThreads = 256;
+constexpr int kMaxVec = 8;          // 16-byte vectors per thread in pf_norm: C*H <= 16384
+
+template <typename T> struct V8;
+template <> struct V8<__nv_bfloat16> {
+  static __device__ __forceinline__ void unpack(const uint4& u, float* o) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { const float2 f = __bfloat1622float2(h[i]); o[2 * i] = f.x; o[2 * i + 1] = f.y; }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* in) {
+    uint4 u;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
+    return u;
+  }
+};
+template <> struct V8<__half> {
+  static __device__ __forceinline__ void unpack(const uint4& u, float* o) {
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) { const float2 f = __half22float2(h[i]); o[2 * i] = f.x; o[2 * i + 1] = f.y; }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* in) {
+    uint4 u;
+    __half2* h = reinterpret_cast<__half2*>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
+    return u;
+  }
+};
+
+template <typename T> __device__ __forceinline__ uint4 ldv(const T* p) { return *reinterpret_cast<const uint4*>(p); }
+template <typename T> __device__ __forceinline__ void stv(T* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
+
+// ---------------------------------------------------------------- pf_norm --
+
+template <typename T, int C>
+__global__ void __launch_bounds__(kNormThreads)
+pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* __restrict__ prev_gate,
+        const T* __restrict__ ns, const T* __restrict__ wi, int H, float eps, float gate_div, float gate_mul,
+        T* __restrict__ sout, T* __restrict__ hn, T* __restrict__ post) {
+  pdl_wait();
+  pdl_trigger();
+  __shared__ float red[C][kNormThreads / 32];
+  __shared__ float inv_s[C];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t b = blockIdx.x;
+  const int CH = C * H, NV = CH / 8, NVH = H / 8;
+  const bool pro = prev_out != nullptr;
+  uint4 sv[kMaxVec];
+  float ss[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) ss[c] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int v = tid + i * kNormThreads;
+    if (v < NV) {
+      const int c = v / NVH, h0 = (v - c * NVH) * 8;
+      const uint4 raw = ldv(streams + b * CH + v * 8);
+      float s[8];
+      V8<T>::unpack(raw, s);
+      if (pro) {
+        float p[8];
+        V8<T>::unpack(ldv(prev_out + b * H + h0), p);
+        const float g = ldf(prev_gate + b * C + c);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s[j] = prologue_s<T>(s[j], g, p[j]);
+        sv[i] = V8<T>::pack(s);
+      } else {
+        sv[i] = raw;
+      }
+      if (sout != nullptr) stv(sout + b * CH + v * 8, sv[i]);
+      float q = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) q = fmaf(s[j], s[j], q);
+#pragma unroll
+      for (int cc = 0; cc < C; ++cc)
+        if (cc == c) ss[cc] += q;
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const float w = warp_sum(ss[c]);
+    if (lane == 0) red[c][warp] = w;
+  }
+  __syncthreads();
+  if (tid < C) {
+    float t = 0.0f;
+    for (int w = 0; w < kNormThreads / 32; ++w) t += red[tid][w];
+    inv_s[tid] = inv_rms(t, H, eps);
+  }
+  __syncthreads();
+  float inj[C];
+#pragma unroll
+  for (int c = 0; c < C; ++c) inj[c] = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int v = tid + i * kNormThreads;
+    if (v < NV) {
+      const int c = v / NVH;
+      float s[8], nsf[8], h[8];
+      V8<T>::unpack(sv[i], s);
+      V8<T>::unpack(ldv(ns + v * 8), nsf);
+      const float iv = inv_s[c];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) h[j] = norm_hn<T>(s[j], iv, nsf[j]);
+      stv(hn + b * CH + v * 8, V8<T>::pack(h));
+      // the 8 inject_weight rows of this vector are 8*C contiguous elements
+      float w[8 * C];
+#pragma unroll
+      for (int q = 0; q < C; ++q) V8<T>::unpack(ldv(wi + static_cast<int64_t>(v) * 8 * C + q * 8), w + 8 * q);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int cc = 0; cc < C; ++cc) inj[cc] = fmaf(h[j], w[j * C + cc], inj[cc]);
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int c = 0; c < C; ++c) {
+    const float w = warp_sum(inj[c]);
+    if (lane == 0) red[c][warp] = w;
+  }
+  __syncthreads();
+  if (tid < C) {
+    float t = 0.0f;
+    for (int w = 0; w < kNormThreads / 32; ++w) t += red[tid][w];
+    stf(post + b * C + tid, post_gate_of<T>(rT<T>(t), gate_div, gate_mul));
+  }
+}
+
+// ------------------------------------------------- tensor-core pipelines --
+
+struct alignas(64) PfDownArgs {
+  CUtensorMap tm_a;  // hn      [rows, C*H], box {64 k, 128 rows}
+  CUtensorMap tm_b;  // down_w  [C*H, R],    box {64 n, 64 k}
+  float* part;       // [ksplit, rows, R] fp32
+  int rows, R, k_per_split, stages;
+};
+
+template <typename T>
+struct alignas(64) PfUpArgs {
+  CUtensorMap tm_a;  // d     [rows, R],   box {64 k, 128 rows}
+  CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
+  const T* hn;       // [rows, C*H]
+  T* pre;            // [rows, H]
+  int rows, C, H, R, stages;
+  float rho;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  const uint32_t a = smem_addr(p);
+  return p + ((1024u - (a & 1023u)) & 1023u);
+}
+
+// Shared state of a pipeline in dynamic shared memory, after the stages.
+struct PipeBars {
+  uint64_t full[4], empty[4], done;
+  uint32_t tmem_base;
+};
+
+__device__ __forceinline__ void pipe_init(PipeBars* pb, int stages) {
+  for (int s = 0; s < stages; ++s) {
+    mbar_init(&pb->full[s], 1);
+    mbar_init(&pb->empty[s], 1);
+  }
+  mbar_init(&pb->done, 1);
+  fence_mbar_init();
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__ PfDownArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int R = a.R, NB = R / 64, S = a.stages;
+  const int stage_bytes = kATileBytes + NB * kBoxBytes;
+  PipeBars* pb = reinterpret_cast<PipeBars*>(smem + S * stage_bytes);
+  const int m0 = blockIdx.x * kBM, ks = blockIdx.y;
+  const int k_begin = ks * a.k_per_split, nk = a.k_per_split / kBK;
+  const uint32_t ncols = R <= 256 ? 256u : 512u;
+
+  if (warp == 0 && lane == 0) {
+    pipe_init(pb, S);
+    tma_prefetch_desc(&a.tm_a);
+    tma_prefetch_desc(&a.tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&pb->tmem_base, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = pb->tmem_base;
+  pdl_wait();
+  pdl_trigger();
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int it = 0; it < nk && ok; ++it) {
+        const int s = it % S;
+        ok = mbar_wait(&pb->empty[s], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
+        if (!ok) break;
+        uint8_t* st = smem + s * stage_bytes;
+        mbar_arrive_expect_tx(&pb->full[s], static_cast<uint32_t>(stage_bytes));
+        const int k = k_begin + it * kBK;
+        tma_load_2d(st, &a.tm_a, k, m0, &pb->full[s]);
+        for (int nb = 0; nb < NB; ++nb) tma_load_2d(st + kATileBytes + nb * kBoxBytes, &a.tm_b, nb * 64, k, &pb->full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int it = 0; it < nk && ok; ++it) {
+        const int s = it % S;
+        ok = mbar_wait(&pb->full[s], (it / S) & 1, &g_pf_wait_timeouts);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t abase = smem_addr(smem + s * stage_bytes), bbase = abase + kATileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
+          for (int n0 = 0; n0 < R; n0 += 256) {
+            const int N = min(256, R - n0);
+            const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
+            mma_f16(tmem + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (it > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&pb->empty[s]);
+      }
+      mma_commit(&pb->done);
+    }
+  } else {
+    ok = mbar_wait(&pb->done, 0, &g_pf_wait_timeouts);
+    tc_fence_after();
+    const int lq = warp & 3, row = lq * 32 + lane;
+    const int64_t grow = m0 + row;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+    for (int c0 = 0; c0 < R; c0 += 16) {
+      float v[16];
+      tmem_ld16(taddr + c0, v);
+      if (grow < a.rows) {
+        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * R + c0);
+        const float qn = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          dst[q] = ok ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]) : make_float4(qn, qn, qn, qn);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, int ksplit, int64_t rows, int R,
+                                              float alpha, T* __restrict__ d) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= rows * R) return;
+  float t = 0.0f;
+  for (int ks = 0; ks < ksplit; ++ks) t += part[ks * rows * R + i];
+  stf(d + i, scaled_silu<T>(rT<T>(t), alpha));
+}
+
+template <typename T, bool BF16>
+__global__ void __launch_bounds__(kTcThreads, 1) pf_up(const __grid_constant__ PfUpArgs<T> a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = a.C, H = a.H, R = a.R, S = a.stages, NT = 64 * C;
+  const int stage_bytes = kATileBytes + C * kBoxBytes;
+  PipeBars* pb = reinterpret_cast<PipeBars*>(smem + S * stage_bytes);
+  const int m0 = blockIdx.x * kBM, h0 = blockIdx.y * 64;
+  const int nk = R / kBK;
+  const uint32_t ncols = NT <= 256 ? 256u : 512u;
+
+  if (warp == 0 && lane == 0) {
+    pipe_init(pb, S);
+    tma_prefetch_desc(&a.tm_a);
+    tma_prefetch_desc(&a.tm_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&pb->tmem_base, ncols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = pb->tmem_base;
+  pdl_wait();
+  pdl_trigger();
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int it = 0; it < nk && ok; ++it) {
+        const int s = it % S;
+        ok = mbar_wait(&pb->empty[s], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
+        if (!ok) break;
+        uint8_t* st = smem + s * stage_bytes;
+        mbar_arrive_expect_tx(&pb->full[s], static_cast<uint32_t>(stage_bytes));
+        const int k = it * kBK;
+        tma_load_2d(st, &a.tm_a, k, m0, &pb->full[s]);
+        for (int c = 0; c < C; ++c) tma_load_2d(st + kATileBytes + c * kBoxBytes, &a.tm_b, c * H + h0, k, &pb->full[s]);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      for (int it = 0; it < nk && ok; ++it) {
+        const int s = it % S;
+        ok = mbar_wait(&pb->full[s], (it / S) & 1, &g_pf_wait_timeouts);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t abase = smem_addr(smem + s * stage_bytes), bbase = abase + kATileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk) {
+          const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
+          for (int n0 = 0; n0 < NT; n0 += 256) {
+            const int N = min(256, NT - n0);
+            const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
+            mma_f16(tmem + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (it > 0 || kk > 0) ? 1u : 0u);
+          }
+        }
+        mma_commit(&pb->empty[s]);
+      }
+      mma_commit(&pb->done);
+    }
+  } else {
+    ok = mbar_wait(&pb->done, 0, &g_pf_wait_timeouts);
+    tc_fence_after();
+    const int lq = warp & 3, row = lq * 32 + lane;
+    const int64_t grow = m0 + row;
+    const bool live = grow < a.rows;
+    const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+    const int64_t CH = static_cast<int64_t>(C) * H;
+    for (int hc = 0; hc < 4; ++hc) {
+      float acc[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+      for (int c = 0; c < C; ++c) {
+        float up[16], hv[16];
+        tmem_ld16(taddr + c * 64 + hc * 16, up);
+        if (live) {
+          const T* hp = a.hn + grow * CH + static_cast<int64_t>(c) * H + h0 + hc * 16;
+          V8<T>::unpack(ldv(hp), hv);
+          V8<T>::unpack(ldv(hp + 8), hv + 8);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float g = rT<T>(sigmoid_acc(rT<T>(up[j])));
+            acc[j] = __fadd_rn(acc[j], __fmul_rn(hv[j], g));
+          }
+        }
+      }
+      if (live) {
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[j]) : __int_as_float(0x7fc00000);
+        T* dst = a.pre + grow * H + h0 + hc * 16;
+        stv(dst, V8<T>::pack(o));
+        stv(dst + 8, V8<T>::pack(o + 8));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+}
+
+// ------------------------------------------------------------------ host --
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2D tiled map over a row-major [outer, inner] tensor of 16-bit elements,
+// box {64, box_outer}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {64, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kSmemBudget = 220 * 1024;
+
+int pick_stages(int stage_bytes) {
+  const int s = (kSmemBudget - 1024 - static_cast<int>(sizeof(PipeBars))) / stage_bytes;
+  return std::max(1, std::min(4, s));
+}
+
+struct PfLayout {
+  size_t hn, part, d, total;
+};
+PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
+  const size_t es = dtype_size(dt), CH = static_cast<size_t>(C) * H;
+  PfLayout L;
+  L.hn = 0;
+  L.part = align_up(L.hn + rows * CH * es, 256);
+  L.d = align_up(L.part + static_cast<size_t>(C) * rows * R * 4, 256);
+  L.total = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);
+  return L;
+}
+
+template <typename T, bool BF16>
+cudaError_t run_prefill(const Problem& p) {
+  const PfLayout WL = pf_layout(p.rows, p.C, p.H, p.R, p.dt);
+  char* ws = static_cast<char*>(p.workspace);
+  T* hn = reinterpret_cast<T*>(ws + WL.hn);
+  float* part = reinterpret_cast<float*>(ws + WL.part);
+  T* d = reinterpret_cast<T*>(ws + WL.d);
+  const int C = p.C, H = p.H, R = p.R, CH = C * H;
+  const int64_t rows = p.rows;
+  cudaError_t e;
+
+  auto norm = [&](auto kern) {
+    return launch_pdl(kern, dim3(static_cast<unsigned>(rows)), dim3(kNormThreads), 0, p.stream, 1u,
+                      static_cast<const T*>(p.streams), static_cast<const T*>(p.prev_out),
+                      static_cast<const T*>(p.prev_gate), static_cast<const T*>(p.norm_scale),
+                      static_cast<const T*>(p.inject_w), H, p.eps, p.gate_div, p.gate_mul,
+                      static_cast<T*>(p.streams_out), hn, static_cast<T*>(p.post_gate));
+  };
+  switch (C) {
+    case 1: e = norm(pf_norm<T, 1>); break;
+    case 2: e = norm(pf_norm<T, 2>); break;
+    case 4: e = norm(pf_norm<T, 4>); break;
+    default: e = norm(pf_norm<T, 8>); break;
+  }
+  if (e != cudaSuccess) return e;
+
+  const unsigned mtiles = static_cast<unsigned>((rows + kBM - 1) / kBM);
+  PfDownArgs da;
+  if (!make_map(&da.tm_a, hn, BF16, CH, rows, kBM) || !make_map(&da.tm_b, p.down_w, BF16, R, CH, 64))
+    return cudaErrorInvalidValue;
+  da.part = part;
+  da.rows = static_cast<int>(rows);
+  da.R = R;
+  da.k_per_split = H;  // one K slice per branch
+  const int dstage = kATileBytes + (R / 64) * kBoxBytes;
+  da.stages = pick_stages(dstage);
+  const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + sizeof(PipeBars);
+  e = ensure_smem<pf_down<BF16>>(dsm);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl(pf_down<BF16>, dim3(mtiles, C), dim3(kTcThreads), dsm, p.stream, 1u, da);
+  if (e != cudaSuccess) return e;
+
+  const int64_t nmid = rows * R;
+  e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((nmid + 255) / 256)), dim3(256), 0, p.stream, 1u,
+                 static_cast<const float*>(part), C, rows, R, p.alpha, d);
+  if (e != cudaSuccess) return e;
+
+  PfUpArgs<T> ua;
+  if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_map(&ua.tm_b, p.up_w, BF16, CH, R, 64))
+    return cudaErrorInvalidValue;
+  ua.hn = hn;
+  ua.pre = static_cast<T*>(p.pre_output);
+  ua.rows = static_cast<int>(rows);
+  ua.C = C; ua.H = H; ua.R = R;
+  ua.rho = p.rho;
+  const int ustage = kATileBytes + C * kBoxBytes;
+  ua.stages = pick_stages(ustage);
+  const size_t usm = 1024 + static_cast<size_t>(ua.stages) * ustage + sizeof(PipeBars);
+  e = ensure_smem<pf_up<T, BF16>>(usm);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(pf_up<T, BF16>, dim3(mtiles, H / 64), dim3(kTcThreads), usm, p.stream, 1u, ua);
+}
+
+}  // namespace
+
+bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
+  if (dt != HC_BF16 && dt != HC_F16) return false;
+  if (rows < 9 || rows > (int64_t{1} << 24)) return false;
+  if (!(C == 1 || C == 2 || C == 4 || C == 8)) return false;
+  if (H % 64 != 0 || R % 64 != 0 || R > 512) return false;
+  if (static_cast<int64_t>(C) * H > kMaxVec * kNormThreads * 8) return false;
+  return encode_fn() != nullptr;
+}
+
+size_t prefill_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
+  return pf_layout(rows, C, H, R, dt).total;
+}
+
+cudaError_t launch_prefill(const Problem& p) {
+  return p.dt == HC_BF16 ? run_prefill<__nv_bfloat16, true>(p) : run_prefill<__half, false>(p);
+}
+
+unsigned int read_pf_wait_timeouts(bool reset) {
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pf_wait_timeouts, sizeof(v)) != cudaSuccess) return 0xffffffffu;
+  if (reset) {
+    const unsigned int z = 0;
+    cudaMemcpyToSymbol(g_pf_wait_timeouts, &z, sizeof(z));
+  }
+  return v;
+}
+
+}  // namespace hc

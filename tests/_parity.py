@@ -1,12 +1,26 @@
 """Helpers for GPU-vs-oracle parity tests.
 
 Tolerance (stated with the block's target): float32 within 1e-5 relative,
-float16 / bfloat16 within 2 ulp of T, at every output element. pre_output is a
-signed sum over the branches and can cancel, where a per-element relative
-bound is ill-posed; an element that misses the plain bound is re-judged
-against the same bound at the condition-aware magnitude
-max(|pre|, |rho| * sum_c |hn * g|) (hn and g from the oracle's trace), and the
-number of such elements is reported. streams_out must match bit for bit.
+float16 / bfloat16 within 2 ulp of T, at every output element. Two situations
+make a per-element bound on pre_output ill-posed, and elements that miss the
+plain bound are re-judged for them, each count reported:
+  1. cancellation: pre_output is a signed sum over the branches, so the bound
+     is applied at the condition-aware magnitude max(|pre|, |rho| sum_c |hn g|);
+  2. intermediate rounding flips: the contract rounds down, d, up, hn and g
+     to T; any accumulation order other than the oracle's sequential one (the
+     tensor cores' fp32 accumulation in particular) moves some fp32 values
+     across a rounding boundary of T, flipping them by one ulp, and a flip
+     propagates. The element then passes if it is within 2 ulp of the
+     condition-aware magnitude plus the first-order effect of a one-ulp flip
+     at every rounding site feeding it, propagated with the oracle's values:
+       dd   = 2 ulp(d) + (SG + |alpha down| SG (1 - SG)) ulp(down)
+       dup  = ulp(up) + dd @ |W_u|
+       dg   = ulp(g) + g (1 - g) dup
+       dpre = |rho| sum_c (|hn| dg + ulp(hn) |g|).
+A flip-driven drift must stay rare: for float16 / bfloat16 at least 85% of
+pre_output elements must be bit-identical to the oracle (a missing rounding
+site or a wrong order shows up as a far lower figure). streams_out must match
+bit for bit.
 """
 from __future__ import annotations
 
@@ -47,8 +61,23 @@ def run_gpu(hc, d, C, attrs, flags=0, want_streams_out=True, device="cuda"):
     return to_codes(pre), to_codes(post), (to_codes(sout) if sout is not None else None)
 
 
-def compare(gpu, ref, dt, C, H, R, attrs, check_streams_out=True):
-    """Assert parity; return a dict of statistics."""
+def flip_bound(t, inputs, dt, rows, C, H, R, attrs):
+    """First-order bound on |pre - oracle pre| from one-ulp flips at the
+    contract's rounding sites (see the module docstring)."""
+    u = lambda x: spacing(x, dt)
+    down, sg, d = (t[k].astype(np.float64) for k in ("down", "SG", "hidden"))
+    up, g, hn = (t[k].astype(np.float64) for k in ("up", "g", "hn"))
+    dd = 2 * u(d) + (np.abs(sg) + np.abs(attrs["silu_alpha"] * down) * sg * (1 - sg)) * u(down)
+    wu = np.abs(inputs["up_w"].to(torch.float64).numpy())
+    dup = u(up) + dd @ wu
+    dg = u(g) + g * (1 - g) * dup
+    hn3, g3, dg3 = hn.reshape(rows, C, H), g.reshape(rows, C, H), dg.reshape(rows, C, H)
+    return abs(attrs["reduction_scale"]) * (np.abs(hn3) * dg3 + u(hn3) * np.abs(g3)).sum(1)
+
+
+def compare(gpu, ref, dt, C, H, R, attrs, check_streams_out=True, inputs=None):
+    """Assert parity; return a dict of statistics. ``inputs`` (the block's
+    input tensors) enables the rounding-flip re-judgement for fp16/bf16."""
     gpre, gpost, gsout = gpu
     opre, opost, osout, tr = ref
     rows = opre.shape[0]
@@ -64,12 +93,20 @@ def compare(gpu, ref, dt, C, H, R, attrs, check_streams_out=True):
     if dt == "f32":
         plain = np.abs(gp - op) <= 1e-5 * np.abs(op)
         aware = np.abs(gp - op) <= 1e-5 * np.maximum(np.abs(op), cond)
+        flips = aware
     else:
         plain = ulp_diff(gpre, opre, dt) <= 2
         aware = np.abs(gp - op) <= 2 * spacing(np.maximum(np.abs(op), cond), dt)
-    ok = plain | aware | np.isnan(op)
+        flips = aware
+        if inputs is not None and not (plain | aware).all():
+            flip_mag = flip_bound(t, inputs, dt, rows, C, H, R, attrs)
+            flips = np.abs(gp - op) <= 2 * spacing(np.maximum(np.abs(op), cond), dt) + flip_mag
+    ok = plain | aware | flips | np.isnan(op)
     stats["pre_bit_identical"] = float((gpre == opre).mean()) if gpre.size else 1.0
     stats["pre_cond_rescued"] = int((~plain & aware).sum())
+    stats["pre_flip_rescued"] = int((~plain & ~aware & flips).sum())
+    if dt != "f32" and gpre.size >= 1000:
+        assert stats["pre_bit_identical"] >= 0.85, f"only {stats['pre_bit_identical']:.3f} of pre_output bit-identical"
     bad = np.argwhere(~ok)
     assert ok.all(), (f"pre_output outside tolerance at {len(bad)} elements, e.g. {bad[:5].tolist()}: "
                       f"gpu {gp[tuple(bad[0])]} oracle {op[tuple(bad[0])]} cond {cond[tuple(bad[0])]}")

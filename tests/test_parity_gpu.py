@@ -40,7 +40,7 @@ def check(hc, rows, C, H, R, dt, prologue=True, attrs=I.QWEN_ATTRS, seed=0, flag
         assert hc.path(rows, C, H, R, TORCH_DT[dt], flags) == expect_path
     gpu = run_gpu(hc, d, C, attrs, flags=flags)
     ref = run_oracle(d, C, dt, attrs)
-    return compare(gpu, ref, dt, C, H, R, attrs)
+    return compare(gpu, ref, dt, C, H, R, attrs, inputs=d)
 
 
 # ------------------------------------------------------------ tiny config --
@@ -105,7 +105,7 @@ def test_prefill_size_sampled_rows(hc, dt, C, H):
     gpre, gpost, gsout = run_gpu(hc, d, C, I.QWEN_ATTRS)
     idx = np.unique(np.concatenate([np.arange(0, rows, 509), [1, rows - 2, rows - 1]]))
     ref = run_oracle(d, C, dt, I.QWEN_ATTRS, rows_idx=torch.from_numpy(idx))
-    compare((gpre[idx], gpost[idx], gsout[idx]), ref, dt, C, H, R, I.QWEN_ATTRS)
+    compare((gpre[idx], gpost[idx], gsout[idx]), ref, dt, C, H, R, I.QWEN_ATTRS, inputs=d)
 
 
 # ----------------------------------------------------------- invariants --
@@ -123,7 +123,7 @@ def test_row_independence_bitwise(hc, rows, flags):
             assert np.array_equal(a[j:j + 1], b)
 
 
-@pytest.mark.parametrize("rows,flags", [(1, 0), (8, 0), (16, 0), (4, 2)])
+@pytest.mark.parametrize("rows,flags", [(1, 0), (8, 0), (16, 0), (4, 2), (300, 0)])
 def test_deterministic_over_20_runs(hc, rows, flags):
     d = I.make_block(rows, 4, 2560, 320, "bf16", seed=6, prologue=True)
     first = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=flags)
@@ -146,7 +146,7 @@ def test_zero_up_and_inject_weights(hc):
     d["up_w"] = torch.zeros_like(d["up_w"])
     d["inject_w"] = torch.zeros_like(d["inject_w"])
     gpu = run_gpu(hc, d, 4, I.QWEN_ATTRS)
-    compare(gpu, run_oracle(d, 4, "bf16", I.QWEN_ATTRS), "bf16", 4, 2560, 320, I.QWEN_ATTRS)
+    compare(gpu, run_oracle(d, 4, "bf16", I.QWEN_ATTRS), "bf16", 4, 2560, 320, I.QWEN_ATTRS, inputs=d)
     post = torch.from_numpy(gpu[1].view(np.int16)).view(torch.bfloat16).float()
     assert torch.all(post == 1.0)  # gate_mul / 2
 
@@ -166,13 +166,13 @@ def test_two_chained_blocks(hc, dt):
     w2 = I.make_weights(C, H, R, dt, seed=9, block=1)
     g1 = run_gpu(hc, d1, C, I.QWEN_ATTRS)
     o1 = run_oracle(d1, C, dt, I.QWEN_ATTRS)
-    compare(g1, o1, dt, C, H, R, I.QWEN_ATTRS)
+    compare(g1, o1, dt, C, H, R, I.QWEN_ATTRS, inputs=d1)
     from _util import from_codes
     g2 = run_gpu(hc, dict(w2, streams=from_codes(g1[2], dt), prev_out=from_codes(g1[0], dt),
                           prev_gate=from_codes(g1[1], dt)), C, I.QWEN_ATTRS)
     o2 = run_oracle(dict(w2, streams=from_codes(o1[2], dt), prev_out=from_codes(o1[0], dt),
                          prev_gate=from_codes(o1[1], dt)), C, dt, I.QWEN_ATTRS)
-    compare(g2, o2, dt, C, H, R, I.QWEN_ATTRS, check_streams_out=False)
+    compare(g2, o2, dt, C, H, R, I.QWEN_ATTRS, check_streams_out=False, inputs=w2)
 
 
 @pytest.mark.parametrize("rows", [1, 8, 64])
@@ -237,7 +237,7 @@ def test_misaligned_pointers_take_general_path(hc):
     out = hc.lowrank_mix(st, *[g[k] for k in KEYS[1:]], num_branches=C, **I.QWEN_ATTRS)
     torch.cuda.synchronize()
     ref = run_oracle(d, C, "bf16", I.QWEN_ATTRS)
-    compare(tuple(to_codes(t) for t in out), ref, "bf16", C, H, R, I.QWEN_ATTRS)
+    compare(tuple(to_codes(t) for t in out), ref, "bf16", C, H, R, I.QWEN_ATTRS, inputs=d)
 
 
 def test_workspace_errors(hc):
@@ -260,3 +260,37 @@ def test_cross_path_agreement(hc):
     b = run_gpu(hc, d, 4, I.QWEN_ATTRS, flags=2)
     assert np.array_equal(a[2], b[2])
     assert (a[0] == b[0]).mean() > 0.8
+
+
+# ------------------------------------------------- prefill (tensor cores) --
+
+PREFILL_SHAPES = [(4, 2560, 320), (8, 1280, 320), (1, 4096, 64), (2, 128, 64), (8, 64, 128), (4, 256, 512)]
+
+
+@pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "C%d_H%d_R%d" % s)
+@pytest.mark.parametrize("rows", [9, 130, 300])
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_prefill_path_shapes(hc, shape, rows, dt):
+    """tcgen05 path: one partial tile, several tiles with a ragged tail."""
+    C, H, R = shape
+    check(hc, rows, C, H, R, dt, seed=17, expect_path=hc.HC_PATH_PREFILL)
+
+
+@pytest.mark.parametrize("prologue", [True, False])
+@pytest.mark.parametrize("attrs", [I.QWEN_ATTRS, ODD_ATTRS], ids=["qwen", "odd"])
+def test_prefill_attributes_and_prologue(hc, prologue, attrs):
+    check(hc, 200, 4, 2560, 320, "bf16", prologue=prologue, attrs=attrs, expect_path=hc.HC_PATH_PREFILL)
+
+
+def test_prefill_row_independence_bitwise(hc):
+    """Within the prefill path a row's bits do not depend on the batch: rows
+    of a 300-row call equal the same rows in 137- and 150-row calls (different
+    tile positions)."""
+    C, H, R = 4, 2560, 320
+    d = I.make_block(300, C, H, R, "bf16", seed=19, prologue=True)
+    full = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    for lo, hi in ((0, 137), (150, 300), (7, 160)):
+        sub = {k: (v[lo:hi] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+        part = run_gpu(hc, sub, C, I.QWEN_ATTRS)
+        for a, b in zip(full, part):
+            assert np.array_equal(a[lo:hi], b)
