@@ -43,18 +43,36 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One potentially-blocking probe: the hardware may suspend the thread for a
+// short, system-defined time while the phase is incomplete.
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* timeouts) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_try(bar, parity)) return true;
     if (clock64() - t0 > kWaitLimitCycles) {
       if (timeouts != nullptr) atomicAdd(timeouts, 1u);
       return false;
     }
-    __nanosleep(64);
   }
+}
+
+// Plain arrive (count 1) on an mbarrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned) from

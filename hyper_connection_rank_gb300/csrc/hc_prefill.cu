@@ -188,7 +188,7 @@ struct alignas(64) PfUpArgs {
   CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
   const T* hn;       // [rows, C*H]
   T* pre;            // [rows, H]
-  int rows, C, H, R, stages;
+  int rows, C, H, R, stages, nbuf;
   float rho;
 };
 
@@ -313,20 +313,46 @@ __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, in
   stf(d + i, scaled_silu<T>(rT<T>(t), alpha));
 }
 
+// Persistent up projection: each CTA walks tiles (128 rows x 64 features of
+// every branch) with a stride of gridDim.x. Two tensor-memory accumulators
+// (when 2 x 64 x C columns fit) let the MMA of the next tile run while eight
+// epilogue warps drain the current one.
+constexpr int kUpEpiWarps = 8;
+constexpr int kUpThreads = 64 + 32 * kUpEpiWarps;
+
+struct UpBars {
+  uint64_t full[4], empty[4], accf[2], acce[2];
+  uint32_t tmem_base;
+};
+
+__host__ __device__ inline uint32_t tmem_cols_for(int n) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(n)) c <<= 1;
+  return c;
+}
+
 template <typename T, bool BF16>
-__global__ void __launch_bounds__(kTcThreads, 1) pf_up(const __grid_constant__ PfUpArgs<T> a) {
+__global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ PfUpArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.C, H = a.H, R = a.R, S = a.stages, NT = 64 * C;
+  const int C = a.C, H = a.H, R = a.R, S = a.stages, NT = 64 * C, nbuf = a.nbuf;
   const int stage_bytes = kATileBytes + C * kBoxBytes;
-  PipeBars* pb = reinterpret_cast<PipeBars*>(smem + S * stage_bytes);
-  const int m0 = blockIdx.x * kBM, h0 = blockIdx.y * 64;
+  UpBars* pb = reinterpret_cast<UpBars*>(smem + S * stage_bytes);
+  const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
   const int nk = R / kBK;
-  const uint32_t ncols = NT <= 256 ? 256u : 512u;
+  const uint32_t ncols = tmem_cols_for(nbuf * NT);
 
   if (warp == 0 && lane == 0) {
-    pipe_init(pb, S);
+    for (int st = 0; st < S; ++st) {
+      mbar_init(&pb->full[st], 1);
+      mbar_init(&pb->empty[st], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&pb->accf[b], 1);
+      mbar_init(&pb->acce[b], kUpEpiWarps);
+    }
+    fence_mbar_init();
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
   }
@@ -340,76 +366,117 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_up(const __grid_constant__ P
   const uint32_t tmem = pb->tmem_base;
   pdl_wait();
   pdl_trigger();
-  bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int it = 0; it < nk && ok; ++it) {
-        const int s = it % S;
-        ok = mbar_wait(&pb->empty[s], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
-        if (!ok) break;
-        uint8_t* st = smem + s * stage_bytes;
-        mbar_arrive_expect_tx(&pb->full[s], static_cast<uint32_t>(stage_bytes));
-        const int k = it * kBK;
-        tma_load_2d(st, &a.tm_a, k, m0, &pb->full[s]);
-        for (int c = 0; c < C; ++c) tma_load_2d(st + kATileBytes + c * kBoxBytes, &a.tm_b, c * H + h0, k, &pb->full[s]);
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % S;
+          ok = mbar_wait(&pb->empty[st], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
+          if (!ok) break;
+          uint8_t* sp = smem + st * stage_bytes;
+          mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(stage_bytes));
+          tma_load_2d(sp, &a.tm_a, kb * kBK, m0, &pb->full[st]);
+          for (int c = 0; c < C; ++c)
+            tma_load_2d(sp + kATileBytes + c * kBoxBytes, &a.tm_b, c * H + h0, kb * kBK, &pb->full[st]);
+        }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      for (int it = 0; it < nk && ok; ++it) {
-        const int s = it % S;
-        ok = mbar_wait(&pb->full[s], (it / S) & 1, &g_pf_wait_timeouts);
+      int it = 0, local = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
+        const int buf = local % nbuf, use = local / nbuf;
+        ok = mbar_wait(&pb->acce[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t abase = smem_addr(smem + s * stage_bytes), bbase = abase + kATileBytes;
+        const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NT);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int st = it % S;
+          ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
-          for (int n0 = 0; n0 < NT; n0 += 256) {
-            const int N = min(256, NT - n0);
-            const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
-            mma_f16(tmem + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 16; ++kk) {
+            const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
+            for (int n0 = 0; n0 < NT; n0 += 256) {
+              const int N = min(256, NT - n0);
+              const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
+              mma_f16(dbase + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (kb > 0 || kk > 0) ? 1u : 0u);
+            }
           }
+          mma_commit(&pb->empty[st]);
         }
-        mma_commit(&pb->empty[s]);
+        mma_commit(&pb->accf[buf]);
       }
-      mma_commit(&pb->done);
     }
   } else {
-    ok = mbar_wait(&pb->done, 0, &g_pf_wait_timeouts);
-    tc_fence_after();
-    const int lq = warp & 3, row = lq * 32 + lane;
-    const int64_t grow = m0 + row;
-    const bool live = grow < a.rows;
-    const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+    // Epilogue: warp (2 + e) reads tensor-memory lane quarter (warp % 4) and
+    // features [32 * (e / 4), +32) of the tile, i.e. two 16-feature chunks.
+    const int ew = warp - 2, lq = warp & 3, half = ew >> 2;
     const int64_t CH = static_cast<int64_t>(C) * H;
-    for (int hc = 0; hc < 4; ++hc) {
-      float acc[16];
+    int local = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+      const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
+      const int buf = local % nbuf, use = local / nbuf;
+      ok = mbar_wait(&pb->accf[buf], use & 1, &g_pf_wait_timeouts) && ok;
+      tc_fence_after();
+      const int64_t grow = m0 + lq * 32 + lane;
+      const bool live = grow < a.rows;
+      const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NT);
+      for (int hc = 2 * half; hc < 2 * half + 2; ++hc) {
+        float acc[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
-      for (int c = 0; c < C; ++c) {
-        float up[16], hv[16];
-        tmem_ld16(taddr + c * 64 + hc * 16, up);
+        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+#pragma unroll
+        for (int c0 = 0; c0 < 8; c0 += 4) {
+          if (c0 >= C) break;
+          // hn of these 16 features in (up to) four branches, issued before
+          // the tensor-memory loads so both latencies overlap
+          uint4 hv[4][2];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if (c0 + cc < C && live) {
+              const T* hp = a.hn + grow * CH + static_cast<int64_t>(c0 + cc) * H + h0 + hc * 16;
+              hv[cc][0] = ldv(hp);
+              hv[cc][1] = ldv(hp + 8);
+            }
+          uint32_t up[4][16];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if (c0 + cc < C) tmem_ld16_nowait(taddr + (c0 + cc) * 64 + hc * 16, up[cc]);
+          tmem_ld_wait();
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            if (c0 + cc < C && live) {
+              float hf[16];
+              V8<T>::unpack(hv[cc][0], hf);
+              V8<T>::unpack(hv[cc][1], hf + 8);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float g = sigmoid_rT<T>(rT<T>(__uint_as_float(up[cc][j])));
+                acc[j] = __fadd_rn(acc[j], __fmul_rn(hf[j], g));
+              }
+            }
+        }
         if (live) {
-          const T* hp = a.hn + grow * CH + static_cast<int64_t>(c) * H + h0 + hc * 16;
-          V8<T>::unpack(ldv(hp), hv);
-          V8<T>::unpack(ldv(hp + 8), hv + 8);
+          float o[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float g = rT<T>(sigmoid_acc(rT<T>(up[j])));
-            acc[j] = __fadd_rn(acc[j], __fmul_rn(hv[j], g));
-          }
+          for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[j]) : __int_as_float(0x7fc00000);
+          T* dst = a.pre + grow * H + h0 + hc * 16;
+          stv(dst, V8<T>::pack(o));
+          stv(dst + 8, V8<T>::pack(o + 8));
         }
       }
-      if (live) {
-        float o[16];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[j]) : __int_as_float(0x7fc00000);
-        T* dst = a.pre + grow * H + h0 + hc * 16;
-        stv(dst, V8<T>::pack(o));
-        stv(dst + 8, V8<T>::pack(o + 8));
-      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pb->acce[buf]);
     }
   }
   tc_fence_before();
@@ -525,11 +592,14 @@ cudaError_t run_prefill(const Problem& p) {
   ua.C = C; ua.H = H; ua.R = R;
   ua.rho = p.rho;
   const int ustage = kATileBytes + C * kBoxBytes;
-  ua.stages = pick_stages(ustage);
-  const size_t usm = 1024 + static_cast<size_t>(ua.stages) * ustage + sizeof(PipeBars);
+  ua.nbuf = (2 * 64 * C <= 512) ? 2 : 1;
+  ua.stages = std::max(1, std::min(4, (kSmemBudget - 1024 - static_cast<int>(sizeof(UpBars))) / ustage));
+  const size_t usm = 1024 + static_cast<size_t>(ua.stages) * ustage + sizeof(UpBars);
   e = ensure_smem<pf_up<T, BF16>>(usm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(pf_up<T, BF16>, dim3(mtiles, H / 64), dim3(kTcThreads), usm, p.stream, 1u, ua);
+  const int n_tiles = static_cast<int>(mtiles) * (H / 64);
+  const int grid = std::max(1, std::min(n_tiles, p.num_sms));
+  return launch_pdl(pf_up<T, BF16>, dim3(grid), dim3(kUpThreads), usm, p.stream, 1u, ua);
 }
 
 }  // namespace
