@@ -12,8 +12,10 @@
 //   pf_mid   : down = rT(sum of the partials in slice order), ScaledSiLU -> d.
 //   pf_up    (tcgen05): up = d @ W_u for a tile of 128 rows x (C branches x
 //            64 features); the epilogue reads the accumulators from tensor
-//            memory and computes g = rT(sigmoid(rT(up))), hn * g, the pre-mix
-//            over the branches in order and pre_output, all in registers.
+//            memory and computes g = rT(sigmoid(rT(up))) (sigmoid_fast: the
+//            sigmoid evaluations dominate this kernel's instruction count),
+//            hn * g, the pre-mix over the branches in order and pre_output,
+//            all in registers.
 //
 // Pipelines: one TMA thread, one MMA thread, four epilogue warps; stage
 // hand-off through mbarriers (all waits bounded, see hc_async.cuh).
@@ -186,6 +188,7 @@ template <typename T>
 struct alignas(64) PfUpArgs {
   CUtensorMap tm_a;  // d     [rows, R],   box {64 k, 128 rows}
   CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
+  CUtensorMap tm_hn; // hn    [rows, C*H], box {64 features, 128 rows}
   const T* hn;       // [rows, C*H]
   T* pre;            // [rows, H]
   int rows, C, H, R, stages, nbuf;
@@ -313,18 +316,24 @@ __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, in
   stf(d + i, scaled_silu<T>(rT<T>(t), alpha));
 }
 
-// Persistent up projection: each CTA walks tiles (128 rows x 64 features of
-// every branch) with a stride of gridDim.x. Two tensor-memory accumulators
-// (when 2 x 64 x C columns fit) let the MMA of the next tile run while eight
-// epilogue warps drain the current one.
+// Persistent up projection. A tile is 128 rows x 64 features; its C branches
+// are processed in groups of (up to) four, one group per unit of work, so an
+// accumulator is at most 4 x 64 = 256 tensor-memory columns and two of them
+// (double buffering) always fit. The epilogue keeps the pre-mix sum of a tile
+// in registers across its groups, adding branches in order 0..C-1. The hn
+// values the epilogue needs come into shared memory by TMA (128-byte swizzle,
+// double-buffered per unit), so no global load sits on the epilogue's path.
 constexpr int kUpEpiWarps = 8;
 constexpr int kUpThreads = 64 + 32 * kUpEpiWarps;
+constexpr int kHnBoxBytes = 128 * 64 * 2;   // one branch: 128 rows x 64 features
+constexpr int kUpStages = 2;
 
 struct UpBars {
-  uint64_t full[4], empty[4], accf[2], acce[2];
+  uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[2], hne[2];
   uint32_t tmem_base;
 };
 
+// Tensor-memory allocations are powers of two of at least 32 columns.
 __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(n)) c <<= 1;
@@ -336,25 +345,30 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.C, H = a.H, R = a.R, S = a.stages, NT = 64 * C, nbuf = a.nbuf;
-  const int stage_bytes = kATileBytes + C * kBoxBytes;
-  UpBars* pb = reinterpret_cast<UpBars*>(smem + S * stage_bytes);
+  const int C = a.C, H = a.H, R = a.R;
+  const int G = (C + 3) / 4, GC = C < 4 ? C : 4;       // groups per tile, branches per group
+  const int stage_bytes = kATileBytes + GC * kBoxBytes;
+  uint8_t* hn_s = smem + kUpStages * stage_bytes;       // [2 buffers][GC][128 rows][64] (swizzled)
+  UpBars* pb = reinterpret_cast<UpBars*>(hn_s + 2 * GC * kHnBoxBytes);
   const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
-  const int nk = R / kBK;
-  const uint32_t ncols = tmem_cols_for(nbuf * NT);
+  const int nk = R / kBK, NG = 64 * GC;
+  const uint32_t ncols = tmem_cols_for(2 * NG);
 
   if (warp == 0 && lane == 0) {
-    for (int st = 0; st < S; ++st) {
+    for (int st = 0; st < kUpStages; ++st) {
       mbar_init(&pb->full[st], 1);
       mbar_init(&pb->empty[st], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pb->accf[b], 1);
       mbar_init(&pb->acce[b], kUpEpiWarps);
+      mbar_init(&pb->hnf[b], 1);
+      mbar_init(&pb->hne[b], kUpEpiWarps);
     }
     fence_mbar_init();
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
+    tma_prefetch_desc(&a.tm_hn);
   }
   if (warp == 1) {
     tmem_alloc(&pb->tmem_base, ncols);
@@ -369,114 +383,125 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
 
   if (warp == 0) {
     if (lane == 0) {
-      int it = 0;
+      int it = 0, unit = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % S;
-          ok = mbar_wait(&pb->empty[st], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
+        for (int g = 0; g < G && ok; ++g, ++unit) {
+          const int buf = unit & 1, use = unit >> 1, c_lo = g * 4, nc = min(4, C - c_lo);
+          ok = mbar_wait(&pb->hne[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
           if (!ok) break;
-          uint8_t* sp = smem + st * stage_bytes;
-          mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(stage_bytes));
-          tma_load_2d(sp, &a.tm_a, kb * kBK, m0, &pb->full[st]);
-          for (int c = 0; c < C; ++c)
-            tma_load_2d(sp + kATileBytes + c * kBoxBytes, &a.tm_b, c * H + h0, kb * kBK, &pb->full[st]);
+          mbar_arrive_expect_tx(&pb->hnf[buf], static_cast<uint32_t>(nc * kHnBoxBytes));
+          for (int cc = 0; cc < nc; ++cc)
+            tma_load_2d(hn_s + (buf * GC + cc) * kHnBoxBytes, &a.tm_hn, (c_lo + cc) * H + h0, m0, &pb->hnf[buf]);
+          for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int st = it % kUpStages;
+            ok = mbar_wait(&pb->empty[st], ((it / kUpStages) & 1) ^ 1, &g_pf_wait_timeouts);
+            if (!ok) break;
+            uint8_t* sp = smem + st * stage_bytes;
+            mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + nc * kBoxBytes));
+            tma_load_2d(sp, &a.tm_a, kb * kBK, m0, &pb->full[st]);
+            for (int cc = 0; cc < nc; ++cc)
+              tma_load_2d(sp + kATileBytes + cc * kBoxBytes, &a.tm_b, (c_lo + cc) * H + h0, kb * kBK, &pb->full[st]);
+          }
         }
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      int it = 0, local = 0;
+      int it = 0, unit = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++local) {
-        const int buf = local % nbuf, use = local / nbuf;
-        ok = mbar_wait(&pb->acce[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NT);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int st = it % S;
-          ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        for (int g = 0; g < G && ok; ++g, ++unit) {
+          const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4), N = 64 * nc;
+          ok = mbar_wait(&pb->acce[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
+          const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NG);
+          for (int kb = 0; kb < nk; ++kb, ++it) {
+            const int st = it % kUpStages;
+            ok = mbar_wait(&pb->full[st], (it / kUpStages) & 1, &g_pf_wait_timeouts);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
-            for (int n0 = 0; n0 < NT; n0 += 256) {
-              const int N = min(256, NT - n0);
-              const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
-              mma_f16(dbase + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (kb > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc_sw128(bbase + kk * 16 * 128, kBoxBytes, 1024);
+              mma_f16(dbase, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (kb > 0 || kk > 0) ? 1u : 0u);
             }
+            mma_commit(&pb->empty[st]);
           }
-          mma_commit(&pb->empty[st]);
+          mma_commit(&pb->accf[buf]);
         }
-        mma_commit(&pb->accf[buf]);
       }
     }
   } else {
-    // Epilogue: warp (2 + e) reads tensor-memory lane quarter (warp % 4) and
-    // features [32 * (e / 4), +32) of the tile, i.e. two 16-feature chunks.
+    // Epilogue: warp (2 + e) owns tensor-memory lane quarter (warp % 4) and
+    // features [32 * (e / 4), +32) of the tile: two 16-feature chunks.
     const int ew = warp - 2, lq = warp & 3, half = ew >> 2;
-    const int64_t CH = static_cast<int64_t>(C) * H;
-    int local = 0;
+    const int row = lq * 32 + lane;
+    int unit = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x, ++local) {
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
-      const int buf = local % nbuf, use = local / nbuf;
-      ok = mbar_wait(&pb->accf[buf], use & 1, &g_pf_wait_timeouts) && ok;
-      tc_fence_after();
-      const int64_t grow = m0 + lq * 32 + lane;
+      const int64_t grow = m0 + row;
       const bool live = grow < a.rows;
-      const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NT);
-      for (int hc = 2 * half; hc < 2 * half + 2; ++hc) {
-        float acc[16];
+      float acc[2][16];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
+      for (int q = 0; q < 2; ++q)
 #pragma unroll
-        for (int c0 = 0; c0 < 8; c0 += 4) {
-          if (c0 >= C) break;
-          // hn of these 16 features in (up to) four branches, issued before
-          // the tensor-memory loads so both latencies overlap
-          uint4 hv[4][2];
+        for (int j = 0; j < 16; ++j) acc[q][j] = 0.0f;
+      for (int g = 0; g < G; ++g, ++unit) {
+        const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4);
+        ok = mbar_wait(&pb->accf[buf], use & 1, &g_pf_wait_timeouts) && ok;
+        ok = mbar_wait(&pb->hnf[buf], use & 1, &g_pf_wait_timeouts) && ok;
+        tc_fence_after();
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NG);
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            if (c0 + cc < C && live) {
-              const T* hp = a.hn + grow * CH + static_cast<int64_t>(c0 + cc) * H + h0 + hc * 16;
-              hv[cc][0] = ldv(hp);
-              hv[cc][1] = ldv(hp + 8);
-            }
+        for (int q = 0; q < 2; ++q) {
+          const int hc = 2 * half + q;
           uint32_t up[4][16];
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
-            if (c0 + cc < C) tmem_ld16_nowait(taddr + (c0 + cc) * 64 + hc * 16, up[cc]);
+            if (cc < nc) tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up[cc]);
           tmem_ld_wait();
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc)
-            if (c0 + cc < C && live) {
+            if (cc < nc) {
+              // row `row` of this branch's hn box; 16-byte chunk j of a row
+              // sits at chunk (j ^ (row & 7)) under the 128-byte swizzle
+              const uint8_t* rb = hn_s + (buf * GC + cc) * kHnBoxBytes + row * 128;
+              const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
+              const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
               float hf[16];
-              V8<T>::unpack(hv[cc][0], hf);
-              V8<T>::unpack(hv[cc][1], hf + 8);
+              V8<T>::unpack(v0, hf);
+              V8<T>::unpack(v1, hf + 8);
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const float g = sigmoid_rT<T>(rT<T>(__uint_as_float(up[cc][j])));
-                acc[j] = __fadd_rn(acc[j], __fmul_rn(hf[j], g));
+                const float gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[cc][j]))));
+                acc[q][j] = __fadd_rn(acc[q][j], __fmul_rn(hf[j], gt));
               }
             }
         }
-        if (live) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&pb->acce[buf]);
+          mbar_arrive(&pb->hne[buf]);
+        }
+      }
+      if (live) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
           float o[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[j]) : __int_as_float(0x7fc00000);
-          T* dst = a.pre + grow * H + h0 + hc * 16;
+          for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[q][j]) : __int_as_float(0x7fc00000);
+          T* dst = a.pre + grow * H + h0 + (2 * half + q) * 16;
           stv(dst, V8<T>::pack(o));
           stv(dst + 8, V8<T>::pack(o + 8));
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&pb->acce[buf]);
     }
   }
   tc_fence_before();
@@ -584,17 +609,19 @@ cudaError_t run_prefill(const Problem& p) {
   if (e != cudaSuccess) return e;
 
   PfUpArgs<T> ua;
-  if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_map(&ua.tm_b, p.up_w, BF16, CH, R, 64))
+  if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_map(&ua.tm_b, p.up_w, BF16, CH, R, 64) ||
+      !make_map(&ua.tm_hn, hn, BF16, CH, rows, kBM))
     return cudaErrorInvalidValue;
   ua.hn = hn;
   ua.pre = static_cast<T*>(p.pre_output);
   ua.rows = static_cast<int>(rows);
   ua.C = C; ua.H = H; ua.R = R;
   ua.rho = p.rho;
-  const int ustage = kATileBytes + C * kBoxBytes;
-  ua.nbuf = (2 * 64 * C <= 512) ? 2 : 1;
-  ua.stages = std::max(1, std::min(4, (kSmemBudget - 1024 - static_cast<int>(sizeof(UpBars))) / ustage));
-  const size_t usm = 1024 + static_cast<size_t>(ua.stages) * ustage + sizeof(UpBars);
+  ua.stages = kUpStages;
+  ua.nbuf = 2;
+  const int GC = C < 4 ? C : 4;
+  const size_t usm = 1024 + static_cast<size_t>(kUpStages) * (kATileBytes + GC * kBoxBytes) +
+                     2 * static_cast<size_t>(GC) * kHnBoxBytes + sizeof(UpBars);
   e = ensure_smem<pf_up<T, BF16>>(usm);
   if (e != cudaSuccess) return e;
   const int n_tiles = static_cast<int>(mtiles) * (H / 64);
