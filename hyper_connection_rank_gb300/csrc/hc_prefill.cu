@@ -3,13 +3,13 @@
 // (tcgen05, fp32 accumulators in tensor memory), fed by TMA tensor copies.
 //
 //   pf_norm  (one CTA per row, CUDA cores): prologue S -> streams_out, the
-//            branch RMS statistic, hn -> workspace, inject = hn @ W_i and
-//            post_gate (C x C*H work per row is too small for a tensor tile).
-//   pf_down  (tcgen05): partial[ks] = hn[:, K_ks] @ W_d[K_ks, :] for the
-//            branch-sized K slices ks, 128-row tiles, W_d read in place as an
-//            MN-major operand. Fixed split by branch, so a row's sums never
-//            depend on the number of rows.
-//   pf_mid   : down = rT(sum of the partials in slice order), ScaledSiLU -> d.
+//            branch RMS statistic, hn -> workspace.
+//   pf_down  (tcgen05): partial[ks] = hn[:, K_ks] @ [W_d | W_i][K_ks, :] for
+//            the branch-sized K slices ks, 128-row tiles, W_d read in place as
+//            an MN-major operand, W_i as 16 extra columns. Fixed split by
+//            branch, so a row's sums never depend on the number of rows.
+//   pf_mid   : down = rT(sum of the partials in slice order), ScaledSiLU -> d;
+//            inject likewise -> post_gate.
 //   pf_up    (tcgen05): up = d @ W_u for a tile of 128 rows x (C branches x
 //            64 features); the epilogue reads the accumulators from tensor
 //            memory and computes g = rT(sigmoid(rT(up))) (sigmoid_fast: the
@@ -42,8 +42,8 @@ constexpr int kBK = 64;             // K per stage = one 128-byte swizzle row
 constexpr int kBoxBytes = 64 * 64 * 2;
 constexpr int kATileBytes = kBM * kBK * 2;
 constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA + TMEM owner, warps 2..5 epilogue
-constexpr int kNormThreads = 256;
-constexpr int kMaxVec = 8;          // 16-byte vectors per thread in pf_norm: C*H <= 16384
+constexpr int kNormVec = 4;         // 16-byte vectors per thread in pf_norm
+constexpr int kNormMaxThreads = 512; // so C*H <= 512 * 4 * 8 = 16384
 
 template <typename T> struct V8;
 template <> struct V8<__nv_bfloat16> {
@@ -81,44 +81,55 @@ template <typename T> __device__ __forceinline__ void stv(T* p, const uint4& u) 
 // ---------------------------------------------------------------- pf_norm --
 
 template <typename T, int C>
-__global__ void __launch_bounds__(kNormThreads)
+__global__ void __launch_bounds__(kNormMaxThreads)
 pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* __restrict__ prev_gate,
-        const T* __restrict__ ns, const T* __restrict__ wi, int H, float eps, float gate_div, float gate_mul,
-        T* __restrict__ sout, T* __restrict__ hn, T* __restrict__ post) {
+        const T* __restrict__ ns, int H, float eps, T* __restrict__ sout, T* __restrict__ hn) {
   pdl_wait();
   pdl_trigger();
-  __shared__ float red[C][kNormThreads / 32];
+  __shared__ float red[C][kNormMaxThreads / 32];
   __shared__ float inv_s[C];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x, nwarps = nthr >> 5;
   const int64_t b = blockIdx.x;
   const int CH = C * H, NV = CH / 8, NVH = H / 8;
   const bool pro = prev_out != nullptr;
-  uint4 sv[kMaxVec];
+  // every load of this thread first (one round trip), then the arithmetic
+  uint4 sv[kNormVec], pv[kNormVec], nv[kNormVec];
+  float gt[kNormVec];
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    const int v = tid + i * nthr;
+    if (v < NV) {
+      const int c = v / NVH, h0 = (v - c * NVH) * 8;
+      sv[i] = ldv(streams + b * CH + v * 8);
+      nv[i] = ldv(ns + v * 8);
+      if (pro) {
+        pv[i] = ldv(prev_out + b * H + h0);
+        gt[i] = ldf(prev_gate + b * C + c);
+      }
+    }
+  }
   float ss[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) ss[c] = 0.0f;
 #pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int v = tid + i * kNormThreads;
+  for (int i = 0; i < kNormVec; ++i) {
+    const int v = tid + i * nthr;
     if (v < NV) {
-      const int c = v / NVH, h0 = (v - c * NVH) * 8;
-      const uint4 raw = ldv(streams + b * CH + v * 8);
-      float s[8];
-      V8<T>::unpack(raw, s);
+      const int c = v / NVH;
       if (pro) {
-        float p[8];
-        V8<T>::unpack(ldv(prev_out + b * H + h0), p);
-        const float g = ldf(prev_gate + b * C + c);
+        float s8[8], p8[8];
+        V8<T>::unpack(sv[i], s8);
+        V8<T>::unpack(pv[i], p8);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s[j] = prologue_s<T>(s[j], g, p[j]);
-        sv[i] = V8<T>::pack(s);
-      } else {
-        sv[i] = raw;
+        for (int j = 0; j < 8; ++j) s8[j] = prologue_s<T>(s8[j], gt[i], p8[j]);
+        sv[i] = V8<T>::pack(s8);
       }
       if (sout != nullptr) stv(sout + b * CH + v * 8, sv[i]);
+      float s8[8];
+      V8<T>::unpack(sv[i], s8);
       float q = 0.0f;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) q = fmaf(s[j], s[j], q);
+      for (int j = 0; j < 8; ++j) q = fmaf(s8[j], s8[j], q);
 #pragma unroll
       for (int cc = 0; cc < C; ++cc)
         if (cc == c) ss[cc] += q;
@@ -132,56 +143,33 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
   __syncthreads();
   if (tid < C) {
     float t = 0.0f;
-    for (int w = 0; w < kNormThreads / 32; ++w) t += red[tid][w];
+    for (int w = 0; w < nwarps; ++w) t += red[tid][w];
     inv_s[tid] = inv_rms(t, H, eps);
   }
   __syncthreads();
-  float inj[C];
 #pragma unroll
-  for (int c = 0; c < C; ++c) inj[c] = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int v = tid + i * kNormThreads;
+  for (int i = 0; i < kNormVec; ++i) {
+    const int v = tid + i * nthr;
     if (v < NV) {
-      const int c = v / NVH;
-      float s[8], nsf[8], h[8];
-      V8<T>::unpack(sv[i], s);
-      V8<T>::unpack(ldv(ns + v * 8), nsf);
-      const float iv = inv_s[c];
+      const float iv = inv_s[v / NVH];
+      float s8[8], n8[8], h8[8];
+      V8<T>::unpack(sv[i], s8);
+      V8<T>::unpack(nv[i], n8);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h[j] = norm_hn<T>(s[j], iv, nsf[j]);
-      stv(hn + b * CH + v * 8, V8<T>::pack(h));
-      // the 8 inject_weight rows of this vector are 8*C contiguous elements
-      float w[8 * C];
-#pragma unroll
-      for (int q = 0; q < C; ++q) V8<T>::unpack(ldv(wi + static_cast<int64_t>(v) * 8 * C + q * 8), w + 8 * q);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-#pragma unroll
-        for (int cc = 0; cc < C; ++cc) inj[cc] = fmaf(h[j], w[j * C + cc], inj[cc]);
+      for (int j = 0; j < 8; ++j) h8[j] = norm_hn<T>(s8[j], iv, n8[j]);
+      stv(hn + b * CH + v * 8, V8<T>::pack(h8));
     }
-  }
-  __syncthreads();
-#pragma unroll
-  for (int c = 0; c < C; ++c) {
-    const float w = warp_sum(inj[c]);
-    if (lane == 0) red[c][warp] = w;
-  }
-  __syncthreads();
-  if (tid < C) {
-    float t = 0.0f;
-    for (int w = 0; w < kNormThreads / 32; ++w) t += red[tid][w];
-    stf(post + b * C + tid, post_gate_of<T>(rT<T>(t), gate_div, gate_mul));
   }
 }
 
 // ------------------------------------------------- tensor-core pipelines --
 
 struct alignas(64) PfDownArgs {
-  CUtensorMap tm_a;  // hn      [rows, C*H], box {64 k, 128 rows}
-  CUtensorMap tm_b;  // down_w  [C*H, R],    box {64 n, 64 k}
-  float* part;       // [ksplit, rows, R] fp32
-  int rows, R, k_per_split, stages;
+  CUtensorMap tm_a;        // hn      [rows, C*H], box {64 k, 128 rows}
+  CUtensorMap tm_b;        // down_w  [C*H, R],    box {64 n, 64 k}
+  const uint16_t* wi;      // inject_w [C*H, C] (16-bit codes)
+  float* part;             // [ksplit, rows, R + 16] fp32: down columns, then inject
+  int rows, R, C, k_per_split, stages;
 };
 
 template <typename T>
@@ -202,7 +190,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 
 // Shared state of a pipeline in dynamic shared memory, after the stages.
 struct PipeBars {
-  uint64_t full[4], empty[4], done;
+  uint64_t full[4], empty[4], done, aux;
   uint32_t tmem_base;
 };
 
@@ -215,20 +203,39 @@ __device__ __forceinline__ void pipe_init(PipeBars* pb, int stages) {
   fence_mbar_init();
 }
 
+// The inject projection rides along as 16 extra N columns: one more 8 KB box
+// per stage holds inject_weight's C columns (the rest zero). Its rows are too
+// narrow for a TMA copy (C * 2 bytes), so the producer warp writes them into
+// the swizzled box itself: K-row kr of a 128-byte-swizzled MN-major box keeps
+// columns 0..7 in 16-byte chunk (kr & 7).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 template <bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__ PfDownArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = a.R, NB = R / 64, S = a.stages;
-  const int stage_bytes = kATileBytes + NB * kBoxBytes;
-  PipeBars* pb = reinterpret_cast<PipeBars*>(smem + S * stage_bytes);
+  const int R = a.R, C = a.C, NB = R / 64, S = a.stages, NTOT = R + 16, NP = R + 16;
+  const int stage_bytes = kATileBytes + (NB + 1) * kBoxBytes;
+  uint8_t* wi_s = smem + S * stage_bytes;                // this CTA's K rows of inject_weight, contiguous
+  const uint32_t wi_bytes = static_cast<uint32_t>(a.k_per_split * C * 2);
+  PipeBars* pb = reinterpret_cast<PipeBars*>(wi_s + ((wi_bytes + 15u) & ~15u));
   const int m0 = blockIdx.x * kBM, ks = blockIdx.y;
   const int k_begin = ks * a.k_per_split, nk = a.k_per_split / kBK;
-  const uint32_t ncols = R <= 256 ? 256u : 512u;
+  const uint32_t ncols = NTOT <= 256 ? 256u : 512u;
 
+  // zero the inject box of every stage once; only its first C columns change
+  for (int st = 0; st < S; ++st) {
+    uint4* z = reinterpret_cast<uint4*>(smem + st * stage_bytes + kATileBytes + NB * kBoxBytes);
+    for (int i = threadIdx.x; i < kBoxBytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     pipe_init(pb, S);
+    mbar_init(&pb->aux, 1);
+    fence_mbar_init();
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
   }
@@ -240,41 +247,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = pb->tmem_base;
+  // inject_weight is never written by the preceding kernel (weights): its
+  // K slice may be copied before the dependency wait
+  if (warp == 0 && lane == 0) {
+    mbar_arrive_expect_tx(&pb->aux, wi_bytes);
+    bulk_g2s(wi_s, a.wi + static_cast<int64_t>(k_begin) * C, wi_bytes, &pb->aux);
+  }
   pdl_wait();
   pdl_trigger();
   bool ok = true;
 
   if (warp == 0) {
-    if (lane == 0) {
-      for (int it = 0; it < nk && ok; ++it) {
-        const int s = it % S;
-        ok = mbar_wait(&pb->empty[s], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
-        if (!ok) break;
-        uint8_t* st = smem + s * stage_bytes;
-        mbar_arrive_expect_tx(&pb->full[s], static_cast<uint32_t>(stage_bytes));
-        const int k = k_begin + it * kBK;
-        tma_load_2d(st, &a.tm_a, k, m0, &pb->full[s]);
-        for (int nb = 0; nb < NB; ++nb) tma_load_2d(st + kATileBytes + nb * kBoxBytes, &a.tm_b, nb * 64, k, &pb->full[s]);
+    if (lane == 0) ok = mbar_wait(&pb->aux, 0, &g_pf_wait_timeouts);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    for (int it = 0; it < nk && ok; ++it) {
+      const int st = it % S;
+      if (lane == 0) ok = mbar_wait(&pb->empty[st], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      uint8_t* sp = smem + st * stage_bytes;
+      const int k = k_begin + it * kBK;
+      uint8_t* ibox = sp + kATileBytes + NB * kBoxBytes;
+      for (int kr = lane; kr < kBK; kr += 32) {
+        const uint16_t* src = reinterpret_cast<const uint16_t*>(wi_s) + static_cast<int64_t>(k - k_begin + kr) * C;
+        uint8_t* dst = ibox + kr * 128 + ((kr & 7) << 4);
+        if (C == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        else if (C == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+        else if (C == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+        else *reinterpret_cast<uint16_t*>(dst) = *src;
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + NB * kBoxBytes));
+        tma_load_2d(sp, &a.tm_a, k, m0, &pb->full[st]);
+        for (int nb = 0; nb < NB; ++nb) tma_load_2d(sp + kATileBytes + nb * kBoxBytes, &a.tm_b, nb * 64, k, &pb->full[st]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       for (int it = 0; it < nk && ok; ++it) {
-        const int s = it % S;
-        ok = mbar_wait(&pb->full[s], (it / S) & 1, &g_pf_wait_timeouts);
+        const int st = it % S;
+        ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t abase = smem_addr(smem + s * stage_bytes), bbase = abase + kATileBytes;
+        const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
-          for (int n0 = 0; n0 < R; n0 += 256) {
-            const int N = min(256, R - n0);
+          for (int n0 = 0; n0 < NTOT; n0 += 256) {
+            const int N = min(256, NTOT - n0);
             const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
             mma_f16(tmem + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (it > 0 || kk > 0) ? 1u : 0u);
           }
         }
-        mma_commit(&pb->empty[s]);
+        mma_commit(&pb->empty[st]);
       }
       mma_commit(&pb->done);
     }
@@ -284,11 +311,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
     const int lq = warp & 3, row = lq * 32 + lane;
     const int64_t grow = m0 + row;
     const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
-    for (int c0 = 0; c0 < R; c0 += 16) {
+    for (int c0 = 0; c0 < NTOT; c0 += 16) {
       float v[16];
       tmem_ld16(taddr + c0, v);
       if (grow < a.rows) {
-        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * R + c0);
+        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * NP + c0);
         const float qn = __int_as_float(0x7fc00000);
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -304,16 +331,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
   }
 }
 
+// down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
+// inject likewise -> post_gate.
 template <typename T>
 __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, int ksplit, int64_t rows, int R,
-                                              float alpha, T* __restrict__ d) {
+                                              int C, Attrs at, T* __restrict__ d, T* __restrict__ post) {
   pdl_wait();
   pdl_trigger();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= rows * R) return;
+  const int W = R + C, NP = R + 16;
+  if (i >= rows * W) return;
+  const int64_t row = i / W;
+  const int col = static_cast<int>(i - row * W);
   float t = 0.0f;
-  for (int ks = 0; ks < ksplit; ++ks) t += part[ks * rows * R + i];
-  stf(d + i, scaled_silu<T>(rT<T>(t), alpha));
+  for (int ks = 0; ks < ksplit; ++ks) t += part[(ks * rows + row) * NP + col];
+  if (col < R) stf(d + row * R + col, scaled_silu<T>(rT<T>(t), at.alpha));
+  else stf(post + row * C + (col - R), post_gate_of<T>(rT<T>(t), at.gate_div, at.gate_mul));
 }
 
 // Persistent up projection. A tile is 128 rows x 64 features; its C branches
@@ -556,7 +589,7 @@ PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   PfLayout L;
   L.hn = 0;
   L.part = align_up(L.hn + rows * CH * es, 256);
-  L.d = align_up(L.part + static_cast<size_t>(C) * rows * R * 4, 256);
+  L.d = align_up(L.part + static_cast<size_t>(C) * rows * (R + 16) * 4, 256);
   L.total = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);
   return L;
 }
@@ -573,11 +606,12 @@ cudaError_t run_prefill(const Problem& p) {
   cudaError_t e;
 
   auto norm = [&](auto kern) {
-    return launch_pdl(kern, dim3(static_cast<unsigned>(rows)), dim3(kNormThreads), 0, p.stream, 1u,
+    const int nv = CH / 8;
+    const unsigned nthr = static_cast<unsigned>(std::max(32, (nv + kNormVec - 1) / kNormVec + 31) / 32 * 32);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(rows)), dim3(nthr), 0, p.stream, 1u,
                       static_cast<const T*>(p.streams), static_cast<const T*>(p.prev_out),
-                      static_cast<const T*>(p.prev_gate), static_cast<const T*>(p.norm_scale),
-                      static_cast<const T*>(p.inject_w), H, p.eps, p.gate_div, p.gate_mul,
-                      static_cast<T*>(p.streams_out), hn, static_cast<T*>(p.post_gate));
+                      static_cast<const T*>(p.prev_gate), static_cast<const T*>(p.norm_scale), H, p.eps,
+                      static_cast<T*>(p.streams_out), hn);
   };
   switch (C) {
     case 1: e = norm(pf_norm<T, 1>); break;
@@ -591,21 +625,25 @@ cudaError_t run_prefill(const Problem& p) {
   PfDownArgs da;
   if (!make_map(&da.tm_a, hn, BF16, CH, rows, kBM) || !make_map(&da.tm_b, p.down_w, BF16, R, CH, 64))
     return cudaErrorInvalidValue;
+  da.wi = static_cast<const uint16_t*>(p.inject_w);
   da.part = part;
   da.rows = static_cast<int>(rows);
   da.R = R;
+  da.C = C;
   da.k_per_split = H;  // one K slice per branch
-  const int dstage = kATileBytes + (R / 64) * kBoxBytes;
-  da.stages = pick_stages(dstage);
-  const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + sizeof(PipeBars);
+  const int dstage = kATileBytes + (R / 64 + 1) * kBoxBytes;
+  const int wi_stage = (H * C * 2 + 15) / 16 * 16;
+  da.stages = std::max(1, std::min(4, (kSmemBudget - 1024 - wi_stage - static_cast<int>(sizeof(PipeBars))) / dstage));
+  const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + wi_stage + sizeof(PipeBars);
   e = ensure_smem<pf_down<BF16>>(dsm);
   if (e != cudaSuccess) return e;
   e = launch_pdl(pf_down<BF16>, dim3(mtiles, C), dim3(kTcThreads), dsm, p.stream, 1u, da);
   if (e != cudaSuccess) return e;
 
-  const int64_t nmid = rows * R;
+  const int64_t nmid = rows * (R + C);
+  const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
   e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((nmid + 255) / 256)), dim3(256), 0, p.stream, 1u,
-                 static_cast<const float*>(part), C, rows, R, p.alpha, d);
+                 static_cast<const float*>(part), C, rows, R, C, at, d, static_cast<T*>(p.post_gate));
   if (e != cudaSuccess) return e;
 
   PfUpArgs<T> ua;
@@ -635,8 +673,8 @@ bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   if (dt != HC_BF16 && dt != HC_F16) return false;
   if (rows < 9 || rows > (int64_t{1} << 24)) return false;
   if (!(C == 1 || C == 2 || C == 4 || C == 8)) return false;
-  if (H % 64 != 0 || R % 64 != 0 || R > 512) return false;
-  if (static_cast<int64_t>(C) * H > kMaxVec * kNormThreads * 8) return false;
+  if (H % 64 != 0 || R % 64 != 0 || R > 448) return false;  // R + 16 inject columns <= 512
+  if (static_cast<int64_t>(C) * H > kNormVec * kNormMaxThreads * 8) return false;
   return encode_fn() != nullptr;
 }
 
