@@ -146,6 +146,8 @@ def run_ours(args, rank, world, local_rank):
         if dist:
             tdist.barrier()
 
+    if args.profile_case == "prefill":
+        return profile_prefill(args, hc, I, dev)
     rows = args.rows
     flags = hc.HC_FLAG_WEIGHTS_STATIC
     assert hc.path(rows, C, H, R, torch.bfloat16, flags) == hc.HC_PATH_DECODE
@@ -253,6 +255,22 @@ def profile_case(args, hc, I, dev, rows, flags):
                        out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
     torch.cuda.synchronize()
     return {"profile_case": f"decode rows={rows} bf16, 4 weight sets, {args.warmup}+{args.steps} eager blocks"}
+
+
+def profile_prefill(args, hc, I, dev):
+    """Profiler case for the prefill path: the 8192-row bf16 block (C=4,
+    H=2560, R=320), warmup + steps eager calls through the public API."""
+    import torch
+    rows = 8192
+    d = I.make_block(rows, C, H, R, "bf16", seed=0, prologue=True, device=dev)
+    ws = torch.empty(hc.workspace_size(rows, C, H, R, torch.bfloat16), dtype=torch.uint8, device=dev)
+    out = (torch.empty(rows, H, dtype=torch.bfloat16, device=dev), torch.empty(rows, C, dtype=torch.bfloat16, device=dev),
+           torch.empty(rows, C * H, dtype=torch.bfloat16, device=dev))
+    for _ in range(args.warmup + args.steps):
+        hc.lowrank_mix(d["streams"], d["norm_scale"], d["down_w"], d["up_w"], d["inject_w"], d["prev_out"],
+                       d["prev_gate"], num_branches=C, out=out, workspace=ws, **QWEN)
+    torch.cuda.synchronize()
+    return {"profile_case": f"prefill rows={rows} bf16, {args.warmup}+{args.steps} eager blocks"}
 
 
 def e2e_measure(args, hc, I, weights, dev, flags):
@@ -485,7 +503,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--rows", type=int, default=1, help="decode rows per block (1..8)")
-    ap.add_argument("--profile-case", action="store_true",
+    ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "prefill"),
                     help="small eager case for profiler captures (not a benchmark result)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -39,7 +39,9 @@ template <typename T> __device__ __forceinline__ float rT(float x) { return Ty<T
 // --------------------------------------------------------------- numerics --
 
 // sigmoid(x) = 1 / (1 + exp(-x)): CUDA's accurate expf, IEEE add and divide.
-__device__ __forceinline__ float sigmoid_acc(float x) {
+// Not inlined: the IEEE divide and expf are ~2 KB of code per copy, and the
+// kernels that call this are bound by instruction fetch, not by call cost.
+static __device__ __noinline__ float sigmoid_acc(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-x)));
 }
 
@@ -117,7 +119,7 @@ template <typename T> __device__ __forceinline__ float prologue_s(float s, float
 }
 
 // RMS statistic: inv = 1 / sqrt(sum / H + eps), correctly rounded steps.
-__device__ __forceinline__ float inv_rms(float sumsq, int H, float eps) {
+static __device__ __noinline__ float inv_rms(float sumsq, int H, float eps) {
   float mean = __fdiv_rn(sumsq, static_cast<float>(H));
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 }
@@ -129,14 +131,14 @@ template <typename T> __device__ __forceinline__ float norm_hn(float s, float in
 
 // ScaledSiLU at its three rounding sites: Z = rT(a*x), SG = rT(sigmoid(Z)),
 // hidden = rT(x * SG). x is the already-rounded down projection.
-template <typename T> __device__ __forceinline__ float scaled_silu(float x, float alpha) {
+template <typename T> __device__ __noinline__ float scaled_silu(float x, float alpha) {
   float z = rT<T>(__fmul_rn(alpha, x));
   float sg = rT<T>(sigmoid_acc(z));
   return rT<T>(__fmul_rn(x, sg));
 }
 
 // post_gate = rT(sigmoid(inject / gate_div) * gate_mul), inject already rounded.
-template <typename T> __device__ __forceinline__ float post_gate_of(float inj, float gate_div, float gate_mul) {
+template <typename T> __device__ __noinline__ float post_gate_of(float inj, float gate_div, float gate_mul) {
   return rT<T>(__fmul_rn(sigmoid_acc(__fdiv_rn(inj, gate_div)), gate_mul));
 }
 

@@ -223,6 +223,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
       bulk_g2s(wd_s, a.wd + static_cast<int64_t>(k0) * R, wbytes, bar);
       bulk_g2s(smem + L.wi, a.wi + static_cast<int64_t>(k0) * C, ibytes, bar);
     }
+    #pragma unroll 1
     for (int i = tid; i < KS / VEC; i += nthr) {
       float f[VEC];
       Vec<T>::unpack(ld16(a.ns + k0 + i * VEC), f);
@@ -241,6 +242,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   float ss[MB];
 #pragma unroll
   for (int b = 0; b < MB; ++b) ss[b] = 0.0f;
+  #pragma unroll 1
   for (int v = tid; v < NVr; v += nthr) {
     uint4 sv[MB], pv[MB];
     float gt[MB];
@@ -289,6 +291,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
     if (hk0 == 0) a.inv_ws[tid * C + c] = iv;
   }
   __syncthreads();
+  #pragma unroll 1
   for (int i = tid; i < B * KS; i += nthr) {
     const int b = i / KS, kk = i - b * KS;
     hn_s[i] = norm_hn<T>(hn_s[i], inv_s[b], ns_s[kk]);
@@ -375,10 +378,12 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
         }
   }
   // inject: one warp per (row, branch), lanes over k, butterfly sum
+  #pragma unroll 1
   for (int p = warp; p < B * C; p += nwarps) {
     const int b = p / C, cc = p - b * C;
     float t = 0.0f;
     if (ok)
+      #pragma unroll 1
       for (int kk = lane; kk < KS; kk += 32) t = fmaf(hn_s[b * KS + kk], ldf(wi_s + kk * C + cc), t);
     t = warp_sum(t);
     if (lane == 0) push(b, R + cc, ok ? t : qnan);
@@ -388,6 +393,7 @@ __global__ void __launch_bounds__(512) dec_down(const DownArgs<T> a) {
   // ---- reduce the received partials of the owned columns in rank order ----
   const int clo = rank * ncr, nmine = max(0, min(NC, clo + ncr) - clo);
   const int cluster_id = slice / CL;
+  #pragma unroll 1
   for (int i = tid; i < B * nmine; i += nthr) {
     const int b = i / nmine, lc = i - b * nmine;
     float x[8];
@@ -435,6 +441,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   {
     const int cpr = static_cast<int>(rowbytes / 16);
     const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wu + col0);
+    #pragma unroll 1
     for (int i = tid; i < R * cpr; i += nthr) {
       const int r = i / cpr, qd = i - r * cpr;
       cp_async16(wu_s + static_cast<size_t>(r) * rowbytes + qd * 16, gsrc + (static_cast<int64_t>(r) * CH) * es + qd * 16);
@@ -442,6 +449,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
     cp_async_commit();
   }
   const int nvh = HS / VEC;
+  #pragma unroll 1
   for (int i = tid; i < B * nvh; i += nthr) {
     const int b = i / nvh, qv = i - b * nvh;
     float sf[VEC];
@@ -456,6 +464,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
 #pragma unroll
     for (int j = 0; j < VEC; ++j) hn_s[b * HS + qv * VEC + j] = sf[j];
   }
+  #pragma unroll 1
   for (int i = tid; i < nvh; i += nthr) {
     float f[VEC];
     Vec<T>::unpack(ld16(a.ns + col0 + i * VEC), f);
@@ -492,63 +501,73 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   const int n_items = B * ng, n_units = n_items * nch;
   const int n_post_units = do_post ? B * C * nch : 0;
   float* psum_s = reinterpret_cast<float*>(csum_s + static_cast<size_t>(n_items) * nch);
+  #pragma unroll 1
   for (int u0 = tid; u0 < n_units + n_post_units; u0 += 2 * nthr) {
-    float4 x[2][8];
-    float y[2][8];
+    // address, stride and count of up to two units, then all their loads
+    const float* base[2];
+    int64_t stride[2];
+    int cnt[2], kind[2], slot[2];
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
       const int u = u0 + k * nthr;
-      const bool post_unit = u >= n_units;
-      const int uu = post_unit ? u - n_units : u;
-      const int nk = post_unit ? B * C : n_items;  // consecutive units: consecutive items of one chunk
-      const int ch = uu / nk, item = uu - ch * nk;
-      const int p_lo = ch * cs;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bool live = u < n_units + n_post_units && j < cs && p_lo + j < NP;
-        x[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        y[k][j] = 0.0f;
-        if (live && !post_unit) {
+      cnt[k] = 0;
+      kind[k] = 0;
+      slot[k] = 0;
+      base[k] = a.part_ws;
+      stride[k] = 0;
+      if (u < n_units + n_post_units) {
+        const bool post_unit = u >= n_units;
+        const int uu = post_unit ? u - n_units : u;
+        const int nk = post_unit ? B * C : n_items;
+        const int ch = uu / nk, item = uu - ch * nk;
+        cnt[k] = min(cs, NP - ch * cs);
+        kind[k] = post_unit ? 2 : 1;
+        slot[k] = ch * nk + item;
+        if (!post_unit) {
           const int b = item / ng, g = g_lo + (item - b * ng);
-          x[k][j] = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP)[g + (p_lo + j) * pstride4];
-        } else if (live) {
-          const int b = item / C, cc = item - b * C;
-          y[k][j] = a.part_ws[(static_cast<int64_t>(p_lo + j) * B + b) * a.NCP + R + cc];
-        }
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int u = u0 + k * nthr;
-      if (u >= n_units + n_post_units) continue;
-      const bool post_unit = u >= n_units;
-      const int uu = post_unit ? u - n_units : u;
-      const int nk = post_unit ? B * C : n_items;  // consecutive units: consecutive items of one chunk
-      const int ch = uu / nk, item = uu - ch * nk;
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-      float ty = 0.0f;
-      const int cnt = min(cs, NP - ch * cs);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < cnt) {
-          t.x += x[k][j].x; t.y += x[k][j].y; t.z += x[k][j].z; t.w += x[k][j].w;
-          ty += y[k][j];
-        }
-      for (int p = 8; p < cnt; ++p) {
-        if (!post_unit) {  // chunks longer than 8: remaining loads one by one
-          const int b = item / ng, g = g_lo + (item - b * ng);
-          const float4 z = reinterpret_cast<const float4*>(a.part_ws + static_cast<int64_t>(b) * a.NCP)[g + (ch * cs + p) * pstride4];
-          t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
+          base[k] = a.part_ws + static_cast<int64_t>(b) * a.NCP + static_cast<int64_t>(ch * cs) * B * a.NCP + 4 * g;
         } else {
           const int b = item / C, cc = item - b * C;
-          ty += a.part_ws[(static_cast<int64_t>(ch * cs + p) * B + b) * a.NCP + R + cc];
+          base[k] = a.part_ws + static_cast<int64_t>(b) * a.NCP + static_cast<int64_t>(ch * cs) * B * a.NCP + R + cc;
+        }
+        stride[k] = static_cast<int64_t>(B) * a.NCP;
+      }
+    }
+    float4 x[2][8];
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        x[k][j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < cnt[k]) {
+          if (kind[k] == 1) x[k][j] = *reinterpret_cast<const float4*>(base[k] + j * stride[k]);
+          else x[k][j].x = base[k][j * stride[k]];
         }
       }
-      if (post_unit) psum_s[ch * (B * C) + item] = ty;
-      else csum_s[ch * n_items + item] = t;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      if (kind[k] == 0) continue;
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < cnt[k]) {
+          t.x += x[k][j].x; t.y += x[k][j].y; t.z += x[k][j].z; t.w += x[k][j].w;
+        }
+#pragma unroll 1
+      for (int j = 8; j < cnt[k]; ++j) {  // chunks longer than 8: remaining loads one by one
+        if (kind[k] == 1) {
+          const float4 z = *reinterpret_cast<const float4*>(base[k] + j * stride[k]);
+          t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
+        } else {
+          t.x += base[k][j * stride[k]];
+        }
+      }
+      if (kind[k] == 2) psum_s[slot[k]] = t.x;
+      else csum_s[slot[k]] = t;
     }
   }
   __syncthreads();
+  #pragma unroll 1
   for (int i = tid; i < n_items; i += nthr) {
     const int b = i / ng, g = g_lo + (i - b * ng);
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -556,8 +575,10 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
       const float4 z = csum_s[ch * n_items + i];
       t.x += z.x; t.y += z.y; t.z += z.z; t.w += z.w;
     }
-    const float4 dv = make_float4(scaled_silu<T>(rT<T>(t.x), a.at.alpha), scaled_silu<T>(rT<T>(t.y), a.at.alpha),
-                                  scaled_silu<T>(rT<T>(t.z), a.at.alpha), scaled_silu<T>(rT<T>(t.w), a.at.alpha));
+    float dd[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll 1
+    for (int j = 0; j < 4; ++j) dd[j] = scaled_silu<T>(rT<T>(dd[j]), a.at.alpha);
+    const float4 dv = make_float4(dd[0], dd[1], dd[2], dd[3]);
     if (a.split_d) {
       for (int pr = 0; pr < C; ++pr)
         *reinterpret_cast<float4*>(cluster.map_shared_rank(d_s, pr) + b * R + g * 4) = dv;
@@ -566,6 +587,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
     }
   }
   if (do_post) {
+    #pragma unroll 1
     for (int i = tid; i < B * C; i += nthr) {
       float t = 0.0f;
       for (int ch = 0; ch < nch; ++ch) t += psum_s[ch * (B * C) + i];
@@ -573,6 +595,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
       stf(a.post + b * C + cc, post_gate_of<T>(rT<T>(t), a.at.gate_div, a.at.gate_mul));
     }
   }
+  #pragma unroll 1
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
     float iv = inv_r[0];
@@ -594,6 +617,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   for (int b = 0; b < MB; ++b)
 #pragma unroll
     for (int j = 0; j < VEC; ++j) acc[b][j] = 0.0f;
+  #pragma unroll 1
   for (int r = rg; r < R; r += RG) {
     float w[VEC];
     Vec<T>::unpack(*reinterpret_cast<const uint4*>(wu_s + static_cast<size_t>(r) * rowbytes + lv * 16), w);
@@ -622,6 +646,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   // ---- up -> g -> hn*g; the pre-mix sums the products over c = 0..C-1 on
   // the rank that finalises the feature (rank j owns features [j*HSc, ...)) ----
   const int HSc = HS / C;
+  #pragma unroll 1
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
     float u = 0.0f;
@@ -637,6 +662,7 @@ __global__ void __launch_bounds__(kUpThreads) dec_up(const UpArgs<T> a) {
   }
   if (C > 1) {
     cluster_sync_all();
+    #pragma unroll 1
     for (int i = tid; i < B * HSc; i += nthr) {
       const int b = i / HSc, hl = i - b * HSc;
       float acc2 = 0.0f;
