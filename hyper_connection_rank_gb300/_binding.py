@@ -27,7 +27,7 @@ DTYPE_CODES = {torch.float32: HC_F32, torch.float16: HC_F16, torch.bfloat16: HC_
 
 # Every symbol include/hc_lowrank_mix.h declares.
 EXPORTS = ("hc_attrs_default", "hc_lowrank_mix_path", "hc_lowrank_mix_workspace_size", "hc_lowrank_mix",
-           "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts")
+           "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts", "hc_debug_sigmoid_exact")
 
 
 class HcAttrs(ctypes.Structure):
@@ -67,6 +67,8 @@ def load_library(path: str = LIB_PATH):
         L.hc_last_error.restype = ctypes.c_char_p
         L.hc_debug_wait_timeouts.argtypes = [ci]
         L.hc_debug_wait_timeouts.restype = ctypes.c_uint
+        L.hc_debug_sigmoid_exact.argtypes = [ci, vp, vp, vp]
+        L.hc_debug_sigmoid_exact.restype = ci
         _lib = L
         return L
 
@@ -164,3 +166,14 @@ def lowrank_mix(streams, norm_scale, down_w, up_w, inject_w, prev_out=None, prev
 
 def debug_wait_timeouts(reset: bool = False) -> int:
     return lib().hc_debug_wait_timeouts(1 if reset else 0)
+
+
+def debug_sigmoid_exact(dt: torch.dtype, device="cuda"):
+    """(fast, accurate) T codes of rT(sigmoid(x)) for all 65536 codes x of dt
+    (float16 or bfloat16), as int16 tensors on `device` (see
+    hc_debug_sigmoid_exact)."""
+    fast = torch.empty(65536, dtype=torch.int16, device=device)
+    acc = torch.empty(65536, dtype=torch.int16, device=device)
+    s = torch.cuda.current_stream(fast.device)
+    check(lib().hc_debug_sigmoid_exact(DTYPE_CODES[dt], _ptr(fast), _ptr(acc), s.cuda_stream))
+    return fast, acc

@@ -214,7 +214,17 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
 /* Diagnostic: number of bounded device waits that gave up since the last
  * reset (normally 0). Synchronises with the device. */
 unsigned int hc_debug_wait_timeouts(int reset) {
-  return hc::read_wait_timeouts(reset != 0) + hc::read_pf_wait_timeouts(reset != 0);
+  return hc::read_wait_timeouts(reset != 0) + hc::read_tc_wait_timeouts(reset != 0) +
+         hc::read_pf_wait_timeouts(reset != 0);
+}
+
+hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_out, struct CUstream_st* stream) {
+  if (dtype != HC_F16 && dtype != HC_BF16) return hc::set_error(HC_ERR_INVALID_ARG, "dtype must be HC_F16 or HC_BF16");
+  if (fast_out == nullptr || acc_out == nullptr) return hc::set_error(HC_ERR_INVALID_ARG, "null output pointer");
+  const cudaError_t e = hc::launch_sigmoid_codes(dtype, static_cast<uint16_t*>(fast_out), static_cast<uint16_t*>(acc_out),
+                                                 reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return hc::set_error(HC_ERR_CUDA, cudaGetErrorString(e));
+  return HC_OK;
 }
 
 }  // extern "C"

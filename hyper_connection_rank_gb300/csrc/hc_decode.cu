@@ -1,5 +1,7 @@
 // Decode path of the low-rank mix block (rows <= 8): two weight-streaming
-// kernels linked by programmatic dependent launch.
+// kernels linked by programmatic dependent launch. These CUDA-core kernels
+// serve fp32 I/O (and any fp16/bf16 shape the tensor-core pair in
+// hc_decode_tc.cu does not take).
 //
 // The block at decode sizes is bound by reading its weights once: down_weight
 // (C*H x R) and up_weight (R x C*H) are 13.2 MB in bf16 at C=4, H=2560,
@@ -103,19 +105,6 @@ template <> struct Vec<float> {
 
 template <typename T> __device__ __forceinline__ uint4 ld16(const T* p) { return *reinterpret_cast<const uint4*>(p); }
 template <typename T> __device__ __forceinline__ void st16(T* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
-
-// Cluster barrier halves. Every CTA of a cluster arrives early (relaxed: no
-// memory ordering) and waits just before its first store into a peer's
-// shared memory, which guarantees that every peer has started.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-// Full cluster barrier: stores into peers' shared memory made before it are
-// visible to them after it.
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 
 __host__ __device__ inline uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
@@ -792,15 +781,17 @@ cudaError_t run_decode(const Problem& p, const DecodeCfg& g) {
 }  // namespace
 
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
-  return decode_cfg(rows, C, H, R, dt, 148).ok;
+  return decode_tc_supported(rows, C, H, R, dt) || decode_cfg(rows, C, H, R, dt, 148).ok;
 }
 
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
+  if (decode_tc_supported(rows, C, H, R, dt)) return decode_tc_workspace(rows, C, H, R, dt, num_sms);
   const DecodeCfg g = decode_cfg(rows, C, H, R, dt, num_sms);
   return g.ok ? dec_layout(rows, C, R, g).total : 0;
 }
 
 cudaError_t launch_decode(const Problem& p) {
+  if (decode_tc_supported(p.rows, p.C, p.H, p.R, p.dt)) return launch_decode_tc(p);
   const DecodeCfg g = decode_cfg(p.rows, p.C, p.H, p.R, p.dt, p.num_sms);
   if (!g.ok) return cudaErrorInvalidValue;
   switch (p.dt) {

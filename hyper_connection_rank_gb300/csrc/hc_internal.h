@@ -38,6 +38,14 @@ cudaError_t launch_general(const Problem& p);
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode(const Problem& p);
+// Tensor-core decode kernels for fp16/bf16 (hc_decode_tc.cu); launch_decode
+// routes the shapes they support to them.
+bool decode_tc_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+size_t decode_tc_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
+cudaError_t launch_decode_tc(const Problem& p);
+unsigned int read_tc_wait_timeouts(bool reset);
+// Every 16-bit code through the fast rounded sigmoid and the accurate one.
+cudaError_t launch_sigmoid_codes(hc_dtype_t dt, uint16_t* fast, uint16_t* acc, cudaStream_t s);
 // Prefill path: many rows, fp16/bf16, tcgen05 contractions (hc_prefill.cu).
 bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t prefill_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt);
@@ -62,6 +70,11 @@ cudaError_t ensure_smem(size_t bytes) {
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && granted[dev].load(std::memory_order_acquire) >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  // Ask for the largest shared-memory carveout: an SM configured for a smaller
+  // one cannot take a CTA of another kernel that needs more until it drains,
+  // which would stop consecutive kernels of a PDL chain from sharing SMs.
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(Kernel, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess && dev >= 0 && dev < 64) {
     size_t cur = granted[dev].load(std::memory_order_acquire);
     while (cur < bytes && !granted[dev].compare_exchange_weak(cur, bytes)) {

@@ -156,6 +156,18 @@ const char* hc_last_error(void);
  * Synchronises with the current device; reset != 0 clears the count. */
 unsigned int hc_debug_wait_timeouts(int reset);
 
+/* Diagnostic, with no counterpart on the page that defines the block: check of
+ * the fast sigmoid the fp16/bf16 kernels use where the contract rounds
+ * sigmoid(z) to T for a z that is itself a value of T (the ScaledSiLU gate and
+ * g). For each of the 65536 codes x of the 16-bit type `dtype` (HC_F16 or
+ * HC_BF16) it writes the T code of that fast rounded sigmoid to fast_out[x]
+ * and the T code of rT(1 / (1 + expf(-x))), evaluated with CUDA's accurate
+ * expf and an IEEE divide, to acc_out[x]; the two arrays must be identical.
+ * fast_out, acc_out: device buffers of 65536 uint16 each, owned by the caller.
+ * Asynchronous on `stream`. HC_ERR_INVALID_ARG for another dtype or a null
+ * pointer, HC_ERR_CUDA if the launch fails. */
+hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_out, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif
