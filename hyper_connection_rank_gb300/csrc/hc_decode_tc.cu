@@ -16,8 +16,8 @@
 //
 //   dec_down_tc (grid = C*H/KS CTAs, clusters of CL consecutive slices of one
 //   branch)
-//     - bulk-copies its KS rows of down_weight into shared memory, one copy per
-//       row into rows padded by 16 bytes (conflict-free ldmatrix), and its
+//     - copies its KS rows of down_weight into shared memory (16-byte cp.async
+//       into rows padded by 16 bytes: conflict-free ldmatrix) and its
 //       inject_weight slice; when the weights are static this happens before
 //       griddepcontrol.wait, so the stream overlaps the previous kernel;
 //     - one pass over branch c of every row: S (prologue), sum of S^2,
@@ -137,7 +137,7 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
   const int R16 = (R + 15) / 16 * 16, WP = 2 * R16 + 16, AP = 2 * KS + 16, NT = R16 / 16 + 1;
   const int TPR = ceil_div(NT, CL);
   DownSmem L;
-  L.bar = 0;   // weights landed
+  L.bar = 0;   // unused
   L.rbar = 8;  // partial sums from the cluster landed
   L.wd = 16;
   L.wis = a16(L.wd + KS * WP);
@@ -174,7 +174,6 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
   const int R16 = (R + 15) / 16 * 16, NT = R16 / 16 + 1, TPR = ceil_div(NT, CL), OC = TPR * 16;
   const int WP = 2 * R16 + 16, AP = 2 * KS + 16;
   const DownSmem L = down_smem(MB, KS, R, C, CL, nwarps);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bar);
   uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + L.rbar);
   const T* wis = reinterpret_cast<const T*>(smem + L.wis);
   T* wie = reinterpret_cast<T*>(smem + L.wie);
@@ -197,7 +196,6 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
   // Barriers are initialised before the cluster arrive, whose wait (below, by
   // every peer) then orders the initialisation before any remote complete_tx.
   if (tid == 0) {
-    mbar_init(bar, 1);
     mbar_init(rbar, 1);
     // every rank (this one included) sends 16 columns x 4 bytes per owned tile and row
     mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(CL * nmine * B * 64));
@@ -212,16 +210,25 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
     for (int k = tid; k < KS; k += nthr)
       *reinterpret_cast<uint4*>(smem + L.wd + static_cast<size_t>(k) * WP + 2 * R) = make_uint4(0, 0, 0, 0);
   __syncthreads();
+  // The weight slice arrives as 16-byte cp.async chunks issued by every
+  // thread into the padded rows (cheap to issue; one bulk copy per row costs
+  // the issuing warp tens of cycles each). The warp that owns the inject tile
+  // copies the inject slice itself.
+  const int w_inj = (NT - 1) % nwarps;
   auto issue_weights = [&]() {
-    if (warp == 0) {
-      if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(KS * R * 2 + KS * C * 2));
-      __syncwarp();
-      #pragma unroll 1
-      for (int k = lane; k < KS; k += 32)
-        bulk_g2s(smem + L.wd + static_cast<size_t>(k) * WP, a.wd + static_cast<int64_t>(k0 + k) * R,
-                 static_cast<uint32_t>(R * 2), bar);
-      if (lane == 0) bulk_g2s(smem + L.wis, a.wi + static_cast<int64_t>(k0) * C, static_cast<uint32_t>(KS * C * 2), bar);
+    const int cpr = R / 8;  // 16-byte chunks per weight row
+    const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wd + static_cast<int64_t>(k0) * R);
+    #pragma unroll 1
+    for (int i = tid; i < KS * cpr; i += nthr) {
+      const int r = i / cpr, qd = i - r * cpr;
+      cp_async16(smem + L.wd + static_cast<size_t>(r) * WP + qd * 16, gsrc + static_cast<size_t>(r) * R * 2 + qd * 16);
     }
+    if (warp == w_inj) {
+      const unsigned char* isrc = reinterpret_cast<const unsigned char*>(a.wi + static_cast<int64_t>(k0) * C);
+      #pragma unroll 1
+      for (int i = lane; i < KS * C * 2 / 16; i += 32) cp_async16(smem + L.wis + i * 16, isrc + i * 16);
+    }
+    cp_async_commit();
     #pragma unroll 1
     for (int i = tid; i < KS / VEC; i += nthr) {
       float f[VEC];
@@ -230,7 +237,21 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
       for (int j = 0; j < VEC; ++j) ns_s[i * VEC + j] = f[j];
     }
   };
-  if (a.weights_static) issue_weights();
+  // inject_weight widened to 16 columns (zeros past C), by the inject warp
+  auto widen_inject = [&]() {
+    cp_async_wait_all();
+    __syncwarp();
+    #pragma unroll 1
+    for (int i = lane; i < KS * 16; i += 32) {
+      const int k = i >> 4, j = i & 15;
+      wie[i] = j < C ? wis[k * C + j] : Ty<T>::from_f(0.0f);
+    }
+    __syncwarp();
+  };
+  if (a.weights_static) {
+    issue_weights();
+    if (warp == w_inj) widen_inject();  // off the critical path: before the wait
+  }
   pdl_wait();
   if (!a.weights_static) issue_weights();
   pdl_trigger();
@@ -301,22 +322,13 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
     const int b = i / KS, kk = i - b * KS;
     ha[b * (AP / 2) + kk] = Ty<T>::from_f(norm_hn<T>(ss[i], inv_s[b], ns_s[kk]));
   }
-  __syncthreads();
-  const bool ok = mbar_wait(bar, 0, &g_tc_wait_timeouts);
+  if (!a.weights_static && warp == w_inj) widen_inject();
+  cp_async_wait_all();
+  __syncthreads();  // the weight slice (and hn) visible to every warp
 
   // ---- [down | inject] for the slice, transposed: out^T (16 columns x rows)
   // = W^T tile (16 x 16 k) * hn^T (16 k x 8 rows). Warp w owns column tiles
-  // w, w + nwarps, ...; the last tile is inject_weight widened to 16 columns
-  // (zeros past C) ----
-  const int w_inj = (NT - 1) % nwarps;
-  if (warp == w_inj) {
-    #pragma unroll 1
-    for (int i = lane; i < KS * 16; i += 32) {
-      const int k = i >> 4, j = i & 15;
-      wie[i] = j < C ? wis[k * C + j] : Ty<T>::from_f(0.0f);
-    }
-    __syncwarp();
-  }
+  // w, w + nwarps, ...; the last tile is the widened inject_weight ----
   const int ntl = warp < NT ? (NT - 1 - warp) / nwarps + 1 : 0;
   float acc[kMaxTilesPerWarp][4];
 #pragma unroll
@@ -378,7 +390,7 @@ __global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
           const int row = 2 * t4 + (e & 1), col = lt * 16 + g + (e >> 1) * 8;
           if (row < B) {
             const uint32_t slot = smem_addr(recv_s + (rank * MB + row) * OC + col);
-            st_async_b32(mapa_shared(slot, ow), __float_as_uint(ok ? acc[j][e] : qnan), rb);
+            st_async_b32(mapa_shared(slot, ow), __float_as_uint(acc[j][e]), rb);
           }
         }
       }
@@ -476,7 +488,10 @@ __global__ void __launch_bounds__(512) dec_up_tc(const UpArgs<T> a) {
   cluster_arrive_relaxed();
   // The up weights and the block inputs are never written by the preceding
   // dec_down_tc, which triggers its dependents only after its own wait:
-  // reading them before griddepcontrol.wait is safe.
+  // reading them before griddepcontrol.wait is safe. The tile is R rows of HS
+  // contiguous elements, CH apart: 16-byte cp.async chunks, consecutive threads
+  // on consecutive chunks of a row (one instruction per 16 bytes is cheaper to
+  // issue here than one bulk copy per row).
   {
     const int cpr = HS / 8;  // 16-byte chunks per weight row
     const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wu + col0);
