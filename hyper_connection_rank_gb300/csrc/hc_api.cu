@@ -215,7 +215,7 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
  * reset (normally 0). Synchronises with the device. */
 unsigned int hc_debug_wait_timeouts(int reset) {
   return hc::read_wait_timeouts(reset != 0) + hc::read_tc_wait_timeouts(reset != 0) +
-         hc::read_pf_wait_timeouts(reset != 0);
+         hc::read_um_wait_timeouts(reset != 0) + hc::read_pf_wait_timeouts(reset != 0);
 }
 
 hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_out, struct CUstream_st* stream) {

@@ -781,16 +781,19 @@ cudaError_t run_decode(const Problem& p, const DecodeCfg& g) {
 }  // namespace
 
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
-  return decode_tc_supported(rows, C, H, R, dt) || decode_cfg(rows, C, H, R, dt, 148).ok;
+  return decode_um_supported(rows, C, H, R, dt) || decode_tc_supported(rows, C, H, R, dt) ||
+         decode_cfg(rows, C, H, R, dt, 148).ok;
 }
 
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
+  if (decode_um_supported(rows, C, H, R, dt)) return decode_um_workspace(rows, C, H, R, dt, num_sms);
   if (decode_tc_supported(rows, C, H, R, dt)) return decode_tc_workspace(rows, C, H, R, dt, num_sms);
   const DecodeCfg g = decode_cfg(rows, C, H, R, dt, num_sms);
   return g.ok ? dec_layout(rows, C, R, g).total : 0;
 }
 
 cudaError_t launch_decode(const Problem& p) {
+  if (decode_um_supported(p.rows, p.C, p.H, p.R, p.dt)) return launch_decode_um(p);
   if (decode_tc_supported(p.rows, p.C, p.H, p.R, p.dt)) return launch_decode_tc(p);
   const DecodeCfg g = decode_cfg(p.rows, p.C, p.H, p.R, p.dt, p.num_sms);
   if (!g.ok) return cudaErrorInvalidValue;

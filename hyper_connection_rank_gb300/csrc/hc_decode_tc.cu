@@ -48,6 +48,7 @@
 #include "hc_common.cuh"
 #include "hc_internal.h"
 #include "hc_mma.cuh"
+#include "hc_vec.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -72,57 +73,6 @@ constexpr int kUpKG = 4;    // dec_up: same
 
 __host__ __device__ inline uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
 __host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
-
-// 16-byte vectors of T <-> 8 floats. bf16 widens by a shift: the value is the
-// top half of an fp32 word.
-template <typename T> struct V8;
-template <> struct V8<__nv_bfloat16> {
-  static __device__ __forceinline__ void unpack(const uint4& u, float* f) {
-    const uint32_t q[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      f[2 * i] = __uint_as_float(q[i] << 16);
-      f[2 * i + 1] = __uint_as_float(q[i] & 0xffff0000u);
-    }
-  }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    uint4 u;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-    return u;
-  }
-};
-template <> struct V8<__half> {
-  static __device__ __forceinline__ void unpack(const uint4& u, float* f) {
-    const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 x = __half22float2(h[i]);
-      f[2 * i] = x.x;
-      f[2 * i + 1] = x.y;
-    }
-  }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    uint4 u;
-    __half2* h = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-    return u;
-  }
-};
-
-template <typename T> __device__ __forceinline__ uint4 ld16(const T* p) { return *reinterpret_cast<const uint4*>(p); }
-template <typename T> __device__ __forceinline__ void st16(T* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
-
-// ScaledSiLU at its three rounding sites, with the sigmoid evaluated by the
-// fast form that reproduces rT(sigmoid_acc(z)) bit for bit (its input z is
-// already a value of T).
-template <typename T> __device__ __forceinline__ float scaled_silu_t(float x, float alpha) {
-  const float z = rT<T>(__fmul_rn(alpha, x));
-  const float sg = sigmoid_rT<T>(z);
-  return rT<T>(__fmul_rn(x, sg));
-}
 
 // ------------------------------------------------------------ dec_down_tc --
 
@@ -163,10 +113,10 @@ struct DownArgs {
   int weights_static;
 };
 
-// At most 512 threads; registers capped so that a CTA of dec_up_tc fits beside
-// it on every SM sub-partition (see the register budget above).
+// At most 512 threads; registers capped at 64 so that a CTA of dec_up_tc fits
+// beside it (see the register budget above).
 template <typename T, int MB>
-__global__ void __maxnreg__(96) dec_down_tc(const DownArgs<T> a) {
+__global__ void __maxnreg__(64) dec_down_tc(const DownArgs<T> a) {
   extern __shared__ __align__(128) unsigned char smem[];
   constexpr int VEC = 8;
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;

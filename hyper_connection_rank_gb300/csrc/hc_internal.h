@@ -44,6 +44,12 @@ bool decode_tc_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_tc_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode_tc(const Problem& p);
 unsigned int read_tc_wait_timeouts(bool reset);
+// tcgen05 decode kernels for fp16/bf16 (hc_decode_um.cu), preferred where
+// they apply (H a multiple of 128, R + 8 <= 512).
+bool decode_um_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
+size_t decode_um_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
+cudaError_t launch_decode_um(const Problem& p);
+unsigned int read_um_wait_timeouts(bool reset);
 // Every 16-bit code through the fast rounded sigmoid and the accurate one.
 cudaError_t launch_sigmoid_codes(hc_dtype_t dt, uint16_t* fast, uint16_t* acc, cudaStream_t s);
 // Prefill path: many rows, fp16/bf16, tcgen05 contractions (hc_prefill.cu).
