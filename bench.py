@@ -126,6 +126,17 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ------------------------------------------------------------ ranks --
+
+def max_over_ranks(x, device):
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as tdist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ------------------------------------------------------------ our arm --
 
 def run_ours(args, rank, world, local_rank):
@@ -198,11 +209,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop() if sampler else None
-    t_ms = ev0.elapsed_time(ev1)
-    if dist:
-        tt = torch.tensor([t_ms], device=dev)
-        tdist.all_reduce(tt, op=tdist.ReduceOp.MAX)
-        t_ms = float(tt.item())
+    t_ms = max_over_ranks(ev0.elapsed_time(ev1), dev) if dist else ev0.elapsed_time(ev1)
     for b in bufs:
         for v in b.values():
             assert torch.isfinite(v.float()).all(), "non-finite values in the chain"
