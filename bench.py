@@ -59,12 +59,17 @@ def peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
-def kernel_source_hash():
+# Sources the decode kernel pair is compiled from: a recorded traffic figure is
+# valid only while these are unchanged.
+DECODE_SOURCES = ("hc_decode_um.cu", "hc_common.cuh", "hc_async.cuh", "hc_tc.cuh", "hc_vec.cuh", "hc_internal.h")
+
+
+def kernel_source_hash(files=DECODE_SOURCES):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "hyper_connection_rank_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in sorted(files):
+        h.update(fn.encode())
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -75,7 +80,7 @@ def recorded_traffic(name):
     if not os.path.exists(p):
         return None
     j = json.load(open(p)).get(name)
-    if not j or j.get("source_hash") != kernel_source_hash():
+    if not j or j.get("source_hash") != kernel_source_hash(tuple(j.get("sources", DECODE_SOURCES))):
         return None
     return j.get("dram_bytes_per_unit")
 

@@ -80,8 +80,10 @@ template <typename T> __device__ __forceinline__ void stv(T* p, const uint4& u) 
 
 // ---------------------------------------------------------------- pf_norm --
 
+// At most 64 registers (3 CTAs of 320 threads per SM): the loads in flight are
+// what keeps this streaming kernel near the copy bandwidth.
 template <typename T, int C>
-__global__ void __launch_bounds__(kNormMaxThreads)
+__global__ void __launch_bounds__(kNormMaxThreads, 2)
 pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* __restrict__ prev_gate,
         const T* __restrict__ ns, int H, float eps, T* __restrict__ sout, T* __restrict__ hn) {
   pdl_wait();
@@ -92,8 +94,9 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
   const int64_t b = blockIdx.x;
   const int CH = C * H, NV = CH / 8, NVH = H / 8;
   const bool pro = prev_out != nullptr;
-  // every load of this thread first (one round trip), then the arithmetic
-  uint4 sv[kNormVec], pv[kNormVec], nv[kNormVec];
+  // every load of this thread first (one round trip), then the arithmetic;
+  // norm_scale (the same for every row, cache-resident) is read at the end
+  uint4 sv[kNormVec], pv[kNormVec];
   float gt[kNormVec];
 #pragma unroll
   for (int i = 0; i < kNormVec; ++i) {
@@ -101,7 +104,6 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
     if (v < NV) {
       const int c = v / NVH, h0 = (v - c * NVH) * 8;
       sv[i] = ldv(streams + b * CH + v * 8);
-      nv[i] = ldv(ns + v * 8);
       if (pro) {
         pv[i] = ldv(prev_out + b * H + h0);
         gt[i] = ldf(prev_gate + b * C + c);
@@ -154,7 +156,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
       const float iv = inv_s[v / NVH];
       float s8[8], n8[8], h8[8];
       V8<T>::unpack(sv[i], s8);
-      V8<T>::unpack(nv[i], n8);
+      V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);
 #pragma unroll
       for (int j = 0; j < 8; ++j) h8[j] = norm_hn<T>(s8[j], iv, n8[j]);
       stv(hn + b * CH + v * 8, V8<T>::pack(h8));
