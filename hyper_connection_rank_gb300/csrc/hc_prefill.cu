@@ -29,6 +29,7 @@
 #include "hc_common.cuh"
 #include "hc_internal.h"
 #include "hc_tc.cuh"
+#include "hc_vec.cuh"
 
 namespace hc {
 
@@ -45,38 +46,6 @@ constexpr int kTcThreads = 192;     // warp 0 TMA, warp 1 MMA + TMEM owner, warp
 constexpr int kNormVec = 4;         // 16-byte vectors per thread in pf_norm
 constexpr int kNormMaxThreads = 512; // so C*H <= 512 * 4 * 8 = 16384
 
-template <typename T> struct V8;
-template <> struct V8<__nv_bfloat16> {
-  static __device__ __forceinline__ void unpack(const uint4& u, float* o) {
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) { const float2 f = __bfloat1622float2(h[i]); o[2 * i] = f.x; o[2 * i + 1] = f.y; }
-  }
-  static __device__ __forceinline__ uint4 pack(const float* in) {
-    uint4 u;
-    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(in[2 * i], in[2 * i + 1]);
-    return u;
-  }
-};
-template <> struct V8<__half> {
-  static __device__ __forceinline__ void unpack(const uint4& u, float* o) {
-    const __half2* h = reinterpret_cast<const __half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) { const float2 f = __half22float2(h[i]); o[2 * i] = f.x; o[2 * i + 1] = f.y; }
-  }
-  static __device__ __forceinline__ uint4 pack(const float* in) {
-    uint4 u;
-    __half2* h = reinterpret_cast<__half2*>(&u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(in[2 * i], in[2 * i + 1]);
-    return u;
-  }
-};
-
-template <typename T> __device__ __forceinline__ uint4 ldv(const T* p) { return *reinterpret_cast<const uint4*>(p); }
-template <typename T> __device__ __forceinline__ void stv(T* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
 
 // ---------------------------------------------------------------- pf_norm --
 
@@ -103,9 +72,9 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
     const int v = tid + i * nthr;
     if (v < NV) {
       const int c = v / NVH, h0 = (v - c * NVH) * 8;
-      sv[i] = ldv(streams + b * CH + v * 8);
+      sv[i] = ld16(streams + b * CH + v * 8);
       if (pro) {
-        pv[i] = ldv(prev_out + b * H + h0);
+        pv[i] = ld16(prev_out + b * H + h0);
         gt[i] = ldf(prev_gate + b * C + c);
       }
     }
@@ -126,7 +95,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
         for (int j = 0; j < 8; ++j) s8[j] = prologue_s<T>(s8[j], gt[i], p8[j]);
         sv[i] = V8<T>::pack(s8);
       }
-      if (sout != nullptr) stv(sout + b * CH + v * 8, sv[i]);
+      if (sout != nullptr) st16(sout + b * CH + v * 8, sv[i]);
       float s8[8];
       V8<T>::unpack(sv[i], s8);
       float q = 0.0f;
@@ -159,7 +128,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
       V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);
 #pragma unroll
       for (int j = 0; j < 8; ++j) h8[j] = norm_hn<T>(s8[j], iv, n8[j]);
-      stv(hn + b * CH + v * 8, V8<T>::pack(h8));
+      st16(hn + b * CH + v * 8, V8<T>::pack(h8));
     }
   }
 }
@@ -335,20 +304,37 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
 
 // down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
 // inject likewise -> post_gate.
+// One thread per 4 down columns (float4 partial loads, one 8-byte store of d)
+// or per inject column. ScaledSiLU's gate uses the fast sigmoid that matches
+// the accurate one bit for bit on T inputs.
 template <typename T>
 __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, int ksplit, int64_t rows, int R,
                                               int C, Attrs at, T* __restrict__ d, T* __restrict__ post) {
   pdl_wait();
   pdl_trigger();
   const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const int W = R + C, NP = R + 16;
+  const int R4 = R / 4, W = R4 + C, NP = R + 16;
   if (i >= rows * W) return;
   const int64_t row = i / W;
-  const int col = static_cast<int>(i - row * W);
-  float t = 0.0f;
-  for (int ks = 0; ks < ksplit; ++ks) t += part[(ks * rows + row) * NP + col];
-  if (col < R) stf(d + row * R + col, scaled_silu<T>(rT<T>(t), at.alpha));
-  else stf(post + row * C + (col - R), post_gate_of<T>(rT<T>(t), at.gate_div, at.gate_mul));
+  const int j = static_cast<int>(i - row * W);
+  if (j < R4) {
+    float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int ks = 0; ks < ksplit; ++ks) {
+      const float4 p = *reinterpret_cast<const float4*>(part + (ks * rows + row) * NP + 4 * j);
+      t.x += p.x; t.y += p.y; t.z += p.z; t.w += p.w;
+    }
+    T o[4];
+    o[0] = Ty<T>::from_f(scaled_silu_t<T>(rT<T>(t.x), at.alpha));
+    o[1] = Ty<T>::from_f(scaled_silu_t<T>(rT<T>(t.y), at.alpha));
+    o[2] = Ty<T>::from_f(scaled_silu_t<T>(rT<T>(t.z), at.alpha));
+    o[3] = Ty<T>::from_f(scaled_silu_t<T>(rT<T>(t.w), at.alpha));
+    *reinterpret_cast<uint2*>(d + row * R + 4 * j) = *reinterpret_cast<const uint2*>(o);
+  } else {
+    const int cc = j - R4;
+    float t = 0.0f;
+    for (int ks = 0; ks < ksplit; ++ks) t += part[(ks * rows + row) * NP + R + cc];
+    stf(post + row * C + cc, post_gate_of<T>(rT<T>(t), at.gate_div, at.gate_mul));
+  }
 }
 
 // Persistent up projection. A tile is 128 rows x 64 features; its C branches
@@ -533,8 +519,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
 #pragma unroll
           for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[q][j]) : __int_as_float(0x7fc00000);
           T* dst = a.pre + grow * H + h0 + (2 * half + q) * 16;
-          stv(dst, V8<T>::pack(o));
-          stv(dst + 8, V8<T>::pack(o + 8));
+          st16(dst, V8<T>::pack(o));
+          st16(dst + 8, V8<T>::pack(o + 8));
         }
       }
     }
@@ -642,7 +628,7 @@ cudaError_t run_prefill(const Problem& p) {
   e = launch_pdl(pf_down<BF16>, dim3(mtiles, C), dim3(kTcThreads), dsm, p.stream, 1u, da);
   if (e != cudaSuccess) return e;
 
-  const int64_t nmid = rows * (R + C);
+  const int64_t nmid = rows * (R / 4 + C);
   const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
   e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((nmid + 255) / 256)), dim3(256), 0, p.stream, 1u,
                  static_cast<const float*>(part), C, rows, R, C, at, d, static_cast<T*>(p.post_gate));
