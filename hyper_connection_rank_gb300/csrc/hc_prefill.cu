@@ -5,9 +5,10 @@
 //   pf_norm  (one CTA per row, CUDA cores): prologue S -> streams_out, the
 //            branch RMS statistic, hn -> workspace.
 //   pf_down  (tcgen05): partial[ks] = hn[:, K_ks] @ [W_d | W_i][K_ks, :] for
-//            the branch-sized K slices ks, 128-row tiles, W_d read in place as
-//            an MN-major operand, W_i as 16 extra columns. Fixed split by
-//            branch, so a row's sums never depend on the number of rows.
+//            the K slices ks, 128-row tiles, W_d read in place as an MN-major
+//            operand, W_i as 16 extra columns. The slices are branch-sized, or
+//            256 wide for batches of up to 512 rows (more CTAs for few tiles);
+//            within each regime a row's sums never depend on the row count.
 //   pf_mid   : down = rT(sum of the partials in slice order), ScaledSiLU -> d;
 //            inject likewise -> post_gate.
 //   pf_up    (tcgen05): up = d @ W_u for a tile of 128 rows x (C branches x
@@ -569,15 +570,31 @@ int pick_stages(int stage_bytes) {
   return std::max(1, std::min(4, s));
 }
 
+// K split of the down projection. Batches of up to kSmallRows rows have few
+// 128-row tiles, so K is cut finer (slices of 256, or the largest of 128/64
+// that divides C*H) to give the tensor-core kernel enough CTAs; larger batches
+// split by branch. Within each regime the split is fixed, so a row's bits do
+// not depend on the batch size; across the boundary the summation order
+// differs (as it does between the decode and prefill paths).
+constexpr int64_t kSmallRows = 512;
+int k_per_split_for(int64_t rows, int C, int H) {
+  if (rows > kSmallRows) return H;
+  const int CH = C * H;
+  for (int ks : {256, 128, 64})
+    if (CH % ks == 0) return std::min(ks, H);
+  return H;
+}
+
 struct PfLayout {
   size_t hn, part, d, total;
 };
 PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   const size_t es = dtype_size(dt), CH = static_cast<size_t>(C) * H;
+  const size_t ksplit = CH / k_per_split_for(rows, C, H);
   PfLayout L;
   L.hn = 0;
   L.part = align_up(L.hn + rows * CH * es, 256);
-  L.d = align_up(L.part + static_cast<size_t>(C) * rows * (R + 16) * 4, 256);
+  L.d = align_up(L.part + ksplit * rows * (R + 16) * 4, 256);
   L.total = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);
   return L;
 }
@@ -618,20 +635,22 @@ cudaError_t run_prefill(const Problem& p) {
   da.rows = static_cast<int>(rows);
   da.R = R;
   da.C = C;
-  da.k_per_split = H;  // one K slice per branch
+  da.k_per_split = k_per_split_for(rows, C, H);
+  const unsigned ksplit = static_cast<unsigned>(CH / da.k_per_split);
   const int dstage = kATileBytes + (R / 64 + 1) * kBoxBytes;
-  const int wi_stage = (H * C * 2 + 15) / 16 * 16;
+  const int wi_stage = (da.k_per_split * C * 2 + 15) / 16 * 16;
   da.stages = std::max(1, std::min(4, (kSmemBudget - 1024 - wi_stage - static_cast<int>(sizeof(PipeBars))) / dstage));
   const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + wi_stage + sizeof(PipeBars);
   e = ensure_smem<pf_down<BF16>>(dsm);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(pf_down<BF16>, dim3(mtiles, C), dim3(kTcThreads), dsm, p.stream, 1u, da);
+  e = launch_pdl(pf_down<BF16>, dim3(mtiles, ksplit), dim3(kTcThreads), dsm, p.stream, 1u, da);
   if (e != cudaSuccess) return e;
 
   const int64_t nmid = rows * (R / 4 + C);
   const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
   e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((nmid + 255) / 256)), dim3(256), 0, p.stream, 1u,
-                 static_cast<const float*>(part), C, rows, R, C, at, d, static_cast<T*>(p.post_gate));
+                 static_cast<const float*>(part), static_cast<int>(ksplit), rows, R, C, at, d,
+                 static_cast<T*>(p.post_gate));
   if (e != cudaSuccess) return e;
 
   PfUpArgs<T> ua;

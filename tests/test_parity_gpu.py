@@ -282,6 +282,21 @@ def test_prefill_attributes_and_prologue(hc, prologue, attrs):
     check(hc, 200, 4, 2560, 320, "bf16", prologue=prologue, attrs=attrs, expect_path=hc.HC_PATH_PREFILL)
 
 
+def test_prefill_large_batch_regime(hc):
+    """Past 512 rows the prefill path splits K by branch (below, 256 wide):
+    parity at 600 rows, and a row's bits equal in calls of 640 and 530 rows
+    (both in that regime)."""
+    C, H, R = 4, 2560, 320
+    check(hc, 600, C, H, R, "bf16", seed=23, expect_path=hc.HC_PATH_PREFILL)
+    d = I.make_block(640, C, H, R, "bf16", seed=29, prologue=True)
+    full = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    for lo, hi in ((0, 530), (110, 640)):
+        sub = {k: (v[lo:hi] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+        part = run_gpu(hc, sub, C, I.QWEN_ATTRS)
+        for a, b in zip(full, part):
+            assert np.array_equal(a[lo:hi], b)
+
+
 def test_prefill_row_independence_bitwise(hc):
     """Within the prefill path a row's bits do not depend on the batch: rows
     of a 300-row call equal the same rows in 137- and 150-row calls (different
