@@ -292,24 +292,36 @@ def e2e_measure(args, hc, I, weights, dev, flags):
     import torch
     rows = 1
     src = I.make_activations(rows, C, H, "bf16", seed=1, block=0, prologue=True, device="cpu")
-    host_in = {k: v.pin_memory() for k, v in src.items()}
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in src.items()}
-    dev_out = (torch.empty(rows, H, dtype=torch.bfloat16, device=dev),
-               torch.empty(rows, C, dtype=torch.bfloat16, device=dev),
-               torch.empty(rows, C * H, dtype=torch.bfloat16, device=dev))
-    host_out = tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dev_out)
+    # The step's inputs live in one pinned host buffer and one device buffer
+    # (streams | prev_out | prev_gate, each 16-byte aligned), its outputs
+    # likewise (pre_output | post_gate | streams_out): one copy each way.
+    def packed(shapes, device, pin):
+        sizes = [int(torch.Size(s).numel()) for s in shapes]
+        offs, o = [], 0
+        for n in sizes:
+            offs.append(o)
+            o += (n + 7) // 8 * 8
+        buf = torch.empty(o, dtype=torch.bfloat16, device=device)
+        if pin:
+            buf = buf.pin_memory()
+        return buf, [buf[a:a + n].view(*s) for a, n, s in zip(offs, sizes, shapes)]
+    in_shapes = [src[k].shape for k in ("streams", "prev_out", "prev_gate")]
+    out_shapes = [(rows, H), (rows, C), (rows, C * H)]
+    host_in_buf, host_in = packed(in_shapes, "cpu", True)
+    for t, k in zip(host_in, ("streams", "prev_out", "prev_gate")):
+        t.copy_(src[k])
+    dev_in_buf, dev_in = packed(in_shapes, dev, False)
+    host_out_buf, host_out = packed(out_shapes, "cpu", True)
+    dev_out_buf, dev_out = packed(out_shapes, dev, False)
     ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
     n = max(1, min(args.steps, args.e2e_steps))
 
     def one(i):
-        for k in ("streams", "prev_out", "prev_gate"):
-            dev_in[k].copy_(host_in[k], non_blocking=True)
+        dev_in_buf.copy_(host_in_buf, non_blocking=True)
         w = weights[i % NSETS]
-        hc.lowrank_mix(dev_in["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
-                       dev_in["prev_out"], dev_in["prev_gate"], num_branches=C, flags=flags, out=dev_out,
-                       workspace=ws, **QWEN)
-        for h, d in zip(host_out, dev_out):
-            h.copy_(d, non_blocking=True)
+        hc.lowrank_mix(dev_in[0], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], dev_in[1], dev_in[2],
+                       num_branches=C, flags=flags, out=tuple(dev_out), workspace=ws, **QWEN)
+        host_out_buf.copy_(dev_out_buf, non_blocking=True)
 
     for i in range(max(3, args.warmup)):
         one(i)
@@ -324,8 +336,8 @@ def e2e_measure(args, hc, I, weights, dev, flags):
     e1.synchronize()
     wall = time.perf_counter() - t0
     t = e0.elapsed_time(e1) / 1000.0
-    bi = sum(v.numel() * v.element_size() for v in host_in.values())
-    bo = sum(v.numel() * v.element_size() for v in host_out)
+    bi = host_in_buf.numel() * host_in_buf.element_size()
+    bo = host_out_buf.numel() * host_out_buf.element_size()
     return {"value": round(rows * n / t, 1), "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "steps": n, "us_per_step": round(1e6 * t / n, 3), "wall_us_per_step": round(1e6 * wall / n, 3),
             "api": "hyper_connection_rank_gb300.lowrank_mix -> hc_lowrank_mix (C ABI), eager launches"}

@@ -152,8 +152,8 @@ def lowrank_mix(streams, norm_scale, down_w, up_w, inject_w, prev_out=None, prev
         sout = torch.empty_like(streams) if want_streams_out else None
     else:
         pre, post, sout = out
-    need = workspace_size(rows, C, H, R, dt, flags)
-    if workspace is None:
+    if workspace is None:  # (a caller's workspace is checked against the requirement by the library)
+        need = workspace_size(rows, C, H, R, dt, flags)
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=streams.device)
     attrs = make_attrs(epsilon, reduction_scale, silu_alpha, gate_div, gate_mul, flags)
     s = torch.cuda.current_stream(streams.device) if stream is None else stream

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdarg>
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 
@@ -49,16 +50,27 @@ bool overlaps(const Span& a, const Span& b) {
 }
 
 // Device check: the library is built for sm_103 only.
+// SM count of the current device, queried once per device (0 = not yet known).
+std::atomic<int> g_sms_of_device[64];
+
 hc_status_t device_info(int* num_sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(HC_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev >= 0 && dev < 64) {
+    const int cached = g_sms_of_device[dev].load(std::memory_order_relaxed);
+    if (cached > 0) {
+      *num_sms = cached;
+      return HC_OK;
+    }
+  }
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (major != 10 || minor != 3)
     return fail(HC_ERR_UNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a", dev, major, minor);
   cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64 && *num_sms > 0) g_sms_of_device[dev].store(*num_sms, std::memory_order_relaxed);
   return HC_OK;
 }
 
