@@ -3,7 +3,10 @@
 // (tcgen05, fp32 accumulators in tensor memory), fed by TMA tensor copies.
 //
 //   pf_norm  (one CTA per row, CUDA cores): prologue S -> streams_out, the
-//            branch RMS statistic, hn -> workspace.
+//            branch RMS statistic, hn -> workspace. hn is stored in tiles of
+//            128 rows x 64 columns, each tile 16 KB of contiguous memory
+//            ([row tile][64-column block][row][column]), so that every
+//            operand box the tensor-core kernels load is one contiguous read.
 //   pf_down  (tcgen05): partial[ks] = hn[:, K_ks] @ [W_d | W_i][K_ks, :] for
 //            the K slices ks, 128-row tiles, W_d read in place as an MN-major
 //            operand, W_i as 16 extra columns. The slices are branch-sized, or
@@ -129,7 +132,9 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
       V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);
 #pragma unroll
       for (int j = 0; j < 8; ++j) h8[j] = norm_hn<T>(s8[j], iv, n8[j]);
-      st16(hn + b * CH + v * 8, V8<T>::pack(h8));
+      // tile (b / 128, v / 8), row b % 128, 16-byte chunk v % 8
+      const int64_t tile = (b >> 7) * (CH >> 6) + (v >> 3);
+      st16(hn + ((tile << 7) + (b & 127)) * 64 + (v & 7) * 8, V8<T>::pack(h8));
     }
   }
 }
@@ -137,19 +142,20 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
 // ------------------------------------------------- tensor-core pipelines --
 
 struct alignas(64) PfDownArgs {
-  CUtensorMap tm_a;        // hn      [rows, C*H], box {64 k, 128 rows}
+  CUtensorMap tm_a;        // hn tiles [row tiles * C*H/64][128][64], box {64 k, 128 rows, 1}
   CUtensorMap tm_b;        // down_w  [C*H, R],    box {64 n, 64 k}
   const uint16_t* wi;      // inject_w [C*H, C] (16-bit codes)
   float* part;             // [ksplit, rows, R + 16] fp32: down columns, then inject
   int rows, R, C, k_per_split, stages;
+  int kblocks;             // C*H / 64: hn tiles per row tile
 };
 
 template <typename T>
 struct alignas(64) PfUpArgs {
   CUtensorMap tm_a;  // d     [rows, R],   box {64 k, 128 rows}
   CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
-  CUtensorMap tm_hn; // hn    [rows, C*H], box {64 features, 128 rows}
-  const T* hn;       // [rows, C*H]
+  CUtensorMap tm_hn; // hn tiles [row tiles * C*H/64][128][64], box {64 features, 128 rows, 1}
+  const T* hn;       // tiled, as tm_hn
   T* pre;            // [rows, H]
   int rows, C, H, R, stages, nbuf;
   float rho;
@@ -252,26 +258,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       __syncwarp();
       if (lane == 0) {
         mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + NB * kBoxBytes));
-        tma_load_2d(sp, &a.tm_a, k, m0, &pb->full[st]);
+        tma_load_3d(sp, &a.tm_a, 0, 0, blockIdx.x * a.kblocks + k / kBK, &pb->full[st]);
         for (int nb = 0; nb < NB; ++nb) tma_load_2d(sp + kATileBytes + nb * kBoxBytes, &a.tm_b, nb * 64, k, &pb->full[st]);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
+      // One thread issues every MMA, so nothing but the issue itself may sit
+      // between two of them: the descriptors of stage 0 are built once and
+      // stepped by constants (a descriptor's address field is the shared
+      // memory address / 16, linear below 256 KB). N = R + 16 columns go as
+      // one MMA of up to 256 columns and one of the rest.
+      const int N0 = min(256, NTOT), N1 = NTOT - N0;
+      const uint32_t id0 = idesc_f16(BF16, kBM, N0, false, true);
+      const uint32_t id1 = idesc_f16(BF16, kBM, N1 > 0 ? N1 : 16, false, true);
+      const uint32_t s0 = smem_addr(smem);
+      const uint64_t ad0 = smem_desc_sw128(s0, 16, 1024);
+      const uint64_t bd0 = smem_desc_sw128(s0 + kATileBytes, kBoxBytes, 1024);
+      const uint64_t bd1 = bd0 + ((4 * kBoxBytes) >> 4);
       for (int it = 0; it < nk && ok; ++it) {
         const int st = it % S;
         ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
+        const uint64_t so = static_cast<uint64_t>((st * stage_bytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
-          const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
-          for (int n0 = 0; n0 < NTOT; n0 += 256) {
-            const int N = min(256, NTOT - n0);
-            const uint64_t bdesc = smem_desc_sw128(bbase + (n0 / 64) * kBoxBytes + kk * 16 * 128, kBoxBytes, 1024);
-            mma_f16(tmem + n0, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (it > 0 || kk > 0) ? 1u : 0u);
-          }
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          const uint64_t adesc = ad0 + so + static_cast<uint64_t>(kk * 2);     // + 32 bytes per K step
+          mma_f16(tmem, adesc, bd0 + so + static_cast<uint64_t>(kk * 128), id0, acc);  // + 16 K rows
+          if (N1 > 0) mma_f16(tmem + 256, adesc, bd1 + so + static_cast<uint64_t>(kk * 128), id1, acc);
         }
         mma_commit(&pb->empty[st]);
       }
@@ -345,7 +361,7 @@ __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, in
 // in registers across its groups, adding branches in order 0..C-1. The hn
 // values the epilogue needs come into shared memory by TMA (128-byte swizzle,
 // double-buffered per unit), so no global load sits on the epilogue's path.
-constexpr int kUpEpiWarps = 8;
+constexpr int kUpEpiWarps = 16;
 constexpr int kUpThreads = 64 + 32 * kUpEpiWarps;
 constexpr int kHnBoxBytes = 128 * 64 * 2;   // one branch: 128 rows x 64 features
 constexpr int kUpStages = 2;
@@ -415,7 +431,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           if (!ok) break;
           mbar_arrive_expect_tx(&pb->hnf[buf], static_cast<uint32_t>(nc * kHnBoxBytes));
           for (int cc = 0; cc < nc; ++cc)
-            tma_load_2d(hn_s + (buf * GC + cc) * kHnBoxBytes, &a.tm_hn, (c_lo + cc) * H + h0, m0, &pb->hnf[buf]);
+            tma_load_3d(hn_s + (buf * GC + cc) * kHnBoxBytes, &a.tm_hn, 0, 0,
+                        (m0 / kBM) * (C * H / 64) + ((c_lo + cc) * H + h0) / 64, &pb->hnf[buf]);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int st = it % kUpStages;
             ok = mbar_wait(&pb->empty[st], ((it / kUpStages) & 1) ^ 1, &g_pf_wait_timeouts);
@@ -433,6 +450,9 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     if (lane == 0) {
       int it = 0, unit = 0;
       bool ok = true;
+      const uint32_t s0 = smem_addr(smem);
+      const uint64_t ad0 = smem_desc_sw128(s0, 16, 1024);
+      const uint64_t bd0 = smem_desc_sw128(s0 + kATileBytes, kBoxBytes, 1024);
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         for (int g = 0; g < G && ok; ++g, ++unit) {
           const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4), N = 64 * nc;
@@ -440,18 +460,18 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           if (!ok) break;
           tc_fence_after();
           const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NG);
+          const uint32_t idn = idesc_f16(BF16, kBM, N, false, true);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int st = it % kUpStages;
             ok = mbar_wait(&pb->full[st], (it / kUpStages) & 1, &g_pf_wait_timeouts);
             if (!ok) break;
             tc_fence_after();
-            const uint32_t abase = smem_addr(smem + st * stage_bytes), bbase = abase + kATileBytes;
+            // descriptors stepped by constants, as in pf_down
+            const uint64_t so = static_cast<uint64_t>((st * stage_bytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint64_t adesc = smem_desc_sw128(abase + kk * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc_sw128(bbase + kk * 16 * 128, kBoxBytes, 1024);
-              mma_f16(dbase, adesc, bdesc, idesc_f16(BF16, kBM, N, false, true), (kb > 0 || kk > 0) ? 1u : 0u);
-            }
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_f16(dbase, ad0 + so + static_cast<uint64_t>(kk * 2), bd0 + so + static_cast<uint64_t>(kk * 128), idn,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&pb->empty[st]);
           }
           mma_commit(&pb->accf[buf]);
@@ -460,8 +480,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     }
   } else {
     // Epilogue: warp (2 + e) owns tensor-memory lane quarter (warp % 4) and
-    // features [32 * (e / 4), +32) of the tile: two 16-feature chunks.
-    const int ew = warp - 2, lq = warp & 3, half = ew >> 2;
+    // the 16-feature chunk e / 4 of the tile; it loads one branch's 16
+    // accumulator columns at a time (few registers, so sixteen warps fit and
+    // hide each other's latency).
+    const int ew = warp - 2, lq = warp & 3, hc = ew >> 2;
     const int row = lq * 32 + lane;
     int unit = 0;
     bool ok = true;
@@ -469,42 +491,32 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
       const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
       const int64_t grow = m0 + row;
       const bool live = grow < a.rows;
-      float acc[2][16];
+      float acc[16];
 #pragma unroll
-      for (int q = 0; q < 2; ++q)
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[q][j] = 0.0f;
+      for (int j = 0; j < 16; ++j) acc[j] = 0.0f;
       for (int g = 0; g < G; ++g, ++unit) {
         const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4);
         ok = mbar_wait(&pb->accf[buf], use & 1, &g_pf_wait_timeouts) && ok;
         ok = mbar_wait(&pb->hnf[buf], use & 1, &g_pf_wait_timeouts) && ok;
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NG);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int hc = 2 * half + q;
-          uint32_t up[4][16];
-#pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            if (cc < nc) tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up[cc]);
+        for (int cc = 0; cc < nc; ++cc) {
+          uint32_t up[16];
+          tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up);
+          // row `row` of this branch's hn box; 16-byte chunk j of a row sits
+          // at chunk (j ^ (row & 7)) under the 128-byte swizzle
+          const uint8_t* rb = hn_s + (buf * GC + cc) * kHnBoxBytes + row * 128;
+          const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
+          const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
+          float hf[16];
+          V8<T>::unpack(v0, hf);
+          V8<T>::unpack(v1, hf + 8);
           tmem_ld_wait();
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc)
-            if (cc < nc) {
-              // row `row` of this branch's hn box; 16-byte chunk j of a row
-              // sits at chunk (j ^ (row & 7)) under the 128-byte swizzle
-              const uint8_t* rb = hn_s + (buf * GC + cc) * kHnBoxBytes + row * 128;
-              const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
-              const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
-              float hf[16];
-              V8<T>::unpack(v0, hf);
-              V8<T>::unpack(v1, hf + 8);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[cc][j]))));
-                acc[q][j] = __fadd_rn(acc[q][j], __fmul_rn(hf[j], gt));
-              }
-            }
+          for (int j = 0; j < 16; ++j) {
+            const float gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
+            acc[j] = __fadd_rn(acc[j], __fmul_rn(hf[j], gt));
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -514,15 +526,12 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
         }
       }
       if (live) {
+        float o[16];
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          float o[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[q][j]) : __int_as_float(0x7fc00000);
-          T* dst = a.pre + grow * H + h0 + (2 * half + q) * 16;
-          st16(dst, V8<T>::pack(o));
-          st16(dst + 8, V8<T>::pack(o + 8));
-        }
+        for (int j = 0; j < 16; ++j) o[j] = ok ? __fmul_rn(a.rho, acc[j]) : __int_as_float(0x7fc00000);
+        T* dst = a.pre + grow * H + h0 + hc * 16;
+        st16(dst, V8<T>::pack(o));
+        st16(dst + 8, V8<T>::pack(o + 8));
       }
     }
   }
@@ -563,6 +572,20 @@ bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map over 16-bit tiles of 128 rows x 64 columns stored contiguously
+// ([tile][row][column]), box = one whole tile, 128-byte swizzle.
+bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, uint64_t tiles) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(kBM), tiles};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(kBM) * 128};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(kBM), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kSmemBudget = 220 * 1024;
 
 int pick_stages(int stage_bytes) {
@@ -592,8 +615,8 @@ PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   const size_t es = dtype_size(dt), CH = static_cast<size_t>(C) * H;
   const size_t ksplit = CH / k_per_split_for(rows, C, H);
   PfLayout L;
-  L.hn = 0;
-  L.part = align_up(L.hn + rows * CH * es, 256);
+  L.hn = 0;  // whole 128-row tiles
+  L.part = align_up(L.hn + static_cast<size_t>((rows + kBM - 1) / kBM) * kBM * CH * es, 256);
   L.d = align_up(L.part + ksplit * rows * (R + 16) * 4, 256);
   L.total = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);
   return L;
@@ -628,7 +651,8 @@ cudaError_t run_prefill(const Problem& p) {
 
   const unsigned mtiles = static_cast<unsigned>((rows + kBM - 1) / kBM);
   PfDownArgs da;
-  if (!make_map(&da.tm_a, hn, BF16, CH, rows, kBM) || !make_map(&da.tm_b, p.down_w, BF16, R, CH, 64))
+  const uint64_t hn_tiles = static_cast<uint64_t>(mtiles) * (CH / 64);
+  if (!make_tile_map(&da.tm_a, hn, BF16, hn_tiles) || !make_map(&da.tm_b, p.down_w, BF16, R, CH, 64))
     return cudaErrorInvalidValue;
   da.wi = static_cast<const uint16_t*>(p.inject_w);
   da.part = part;
@@ -636,6 +660,7 @@ cudaError_t run_prefill(const Problem& p) {
   da.R = R;
   da.C = C;
   da.k_per_split = k_per_split_for(rows, C, H);
+  da.kblocks = CH / 64;
   const unsigned ksplit = static_cast<unsigned>(CH / da.k_per_split);
   const int dstage = kATileBytes + (R / 64 + 1) * kBoxBytes;
   const int wi_stage = (da.k_per_split * C * 2 + 15) / 16 * 16;
@@ -655,7 +680,7 @@ cudaError_t run_prefill(const Problem& p) {
 
   PfUpArgs<T> ua;
   if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_map(&ua.tm_b, p.up_w, BF16, CH, R, 64) ||
-      !make_map(&ua.tm_hn, hn, BF16, CH, rows, kBM))
+      !make_tile_map(&ua.tm_hn, hn, BF16, hn_tiles))
     return cudaErrorInvalidValue;
   ua.hn = hn;
   ua.pre = static_cast<T*>(p.pre_output);
