@@ -143,11 +143,13 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
 
 struct alignas(64) PfDownArgs {
   CUtensorMap tm_a;        // hn tiles [row tiles * C*H/64][128][64], box {64 k, 128 rows, 1}
-  CUtensorMap tm_b;        // down_w  [C*H, R],    box {64 n, 64 k}
+  CUtensorMap tm_b;        // down_w viewed as [R/64 column chunks][C*H rows][64 columns],
+                           // box {64 columns, 64 / cs rows, R/64 chunks}
   const uint16_t* wi;      // inject_w [C*H, C] (16-bit codes)
   float* part;             // [ksplit, rows, R + 16] fp32: down columns, then inject
   int rows, R, C, k_per_split, stages;
   int kblocks;             // C*H / 64: hn tiles per row tile
+  int cs;                  // cluster size along the row tiles (1, 2 or 4)
 };
 
 template <typename T>
@@ -181,37 +183,59 @@ __device__ __forceinline__ void pipe_init(PipeBars* pb, int stages) {
   fence_mbar_init();
 }
 
-// The inject projection rides along as 16 extra N columns: one more 8 KB box
-// per stage holds inject_weight's C columns (the rest zero). Its rows are too
-// narrow for a TMA copy (C * 2 bytes), so the producer warp writes them into
-// the swizzled box itself: K-row kr of a 128-byte-swizzled MN-major box keeps
-// columns 0..7 in 16-byte chunk (kr & 7).
+// The inject projection rides along as 16 extra N columns (chunk R/64 of
+// the B operand, C columns used, the rest zero). Its rows are too narrow for
+// a TMA copy (C * 2 bytes), so the producer warp writes them into the
+// swizzled chunk itself: K-row r of a 128-byte-swizzled MN-major chunk keeps
+// columns 0..7 in 16-byte slot (r & 7).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Row tiles that share a K slice run as clusters of `cs` CTAs: the W_d slab
+// of a stage (64 K rows x R columns) is the same for all of them, so cluster
+// rank p loads K rows [p * 64/cs, (p+1) * 64/cs) of it once and multicasts
+// them to every CTA of the cluster; each CTA releases a stage to all of them
+// (commit multicast), so the empty barriers count cs arrivals. L2 delivers
+// the weights once per cluster instead of once per CTA.
+//
+// Shared memory of a stage: the A tile (16 KB), then the B operand as
+// [part p < cs][chunk j <= R/64][64/cs K rows][128 bytes], chunk R/64 being
+// the inject columns. A stage's B operand for K rows [16 kk, 16 kk + 16) sits
+// in one part, so each MMA reads one part with chunk stride (64/cs) * 128.
 template <bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__ PfDownArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = a.R, C = a.C, NB = R / 64, S = a.stages, NTOT = R + 16, NP = R + 16;
-  const int stage_bytes = kATileBytes + (NB + 1) * kBoxBytes;
-  uint8_t* wi_s = smem + S * stage_bytes;                // this CTA's K rows of inject_weight, contiguous
+  const int R = a.R, C = a.C, NB = R / 64, S = a.stages, NTOT = R + 16, NP = R + 16, CS = a.cs;
+  const int prow = kBK / CS;                                        // K rows per part
+  const uint32_t chunk_bytes = static_cast<uint32_t>(prow) * 128u;
+  const uint32_t part_bytes = static_cast<uint32_t>(NB + 1) * chunk_bytes;
+  const int stage_bytes = kATileBytes + (NB + 1) * kBoxBytes;     // A + CS parts
+  uint8_t* wi_s = smem + S * stage_bytes;                           // this CTA's K rows of inject_weight
   const uint32_t wi_bytes = static_cast<uint32_t>(a.k_per_split * C * 2);
   PipeBars* pb = reinterpret_cast<PipeBars*>(wi_s + ((wi_bytes + 15u) & ~15u));
+  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
+  const uint16_t mask = static_cast<uint16_t>((1u << CS) - 1u);
   const int m0 = blockIdx.x * kBM, ks = blockIdx.y;
   const int k_begin = ks * a.k_per_split, nk = a.k_per_split / kBK;
   const uint32_t ncols = NTOT <= 256 ? 256u : 512u;
 
-  // zero the inject box of every stage once; only its first C columns change
-  for (int st = 0; st < S; ++st) {
-    uint4* z = reinterpret_cast<uint4*>(smem + st * stage_bytes + kATileBytes + NB * kBoxBytes);
-    for (int i = threadIdx.x; i < kBoxBytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
-  }
+  // zero the inject chunk of every part of every stage once; only its first
+  // C columns change
+  for (int st = 0; st < S; ++st)
+    for (int p = 0; p < CS; ++p) {
+      uint4* z = reinterpret_cast<uint4*>(smem + st * stage_bytes + kATileBytes + p * part_bytes + NB * chunk_bytes);
+      for (uint32_t i = threadIdx.x; i < chunk_bytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
   fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
-    pipe_init(pb, S);
+    for (int st = 0; st < S; ++st) {
+      mbar_init(&pb->full[st], 1);
+      mbar_init(&pb->empty[st], static_cast<uint32_t>(CS));
+    }
+    mbar_init(&pb->done, 1);
     mbar_init(&pb->aux, 1);
     fence_mbar_init();
     tma_prefetch_desc(&a.tm_a);
@@ -224,6 +248,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA's barriers exist before any peer multicasts into it
+  if (CS > 1) cluster_sync_all();
   const uint32_t tmem = pb->tmem_base;
   // inject_weight is never written by the preceding kernel (weights): its
   // K slice may be copied before the dependency wait
@@ -244,11 +270,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       uint8_t* sp = smem + st * stage_bytes;
+      uint8_t* bsp = sp + kATileBytes;
       const int k = k_begin + it * kBK;
-      uint8_t* ibox = sp + kATileBytes + NB * kBoxBytes;
       for (int kr = lane; kr < kBK; kr += 32) {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(wi_s) + static_cast<int64_t>(k - k_begin + kr) * C;
-        uint8_t* dst = ibox + kr * 128 + ((kr & 7) << 4);
+        const int p = kr / prow, r = kr - p * prow;
+        uint8_t* dst = bsp + p * part_bytes + NB * chunk_bytes + r * 128 + ((r & 7) << 4);
         if (C == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
         else if (C == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
         else if (C == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
@@ -259,7 +286,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       if (lane == 0) {
         mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + NB * kBoxBytes));
         tma_load_3d(sp, &a.tm_a, 0, 0, blockIdx.x * a.kblocks + k / kBK, &pb->full[st]);
-        for (int nb = 0; nb < NB; ++nb) tma_load_2d(sp + kATileBytes + nb * kBoxBytes, &a.tm_b, nb * 64, k, &pb->full[st]);
+        if (CS > 1)
+          tma_load_3d_mc(bsp + rank * part_bytes, &a.tm_b, 0, k + static_cast<int>(rank) * prow, 0, &pb->full[st], mask);
+        else
+          tma_load_3d(bsp, &a.tm_b, 0, k, 0, &pb->full[st]);
       }
     }
   } else if (warp == 1) {
@@ -274,8 +304,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       const uint32_t id1 = idesc_f16(BF16, kBM, N1 > 0 ? N1 : 16, false, true);
       const uint32_t s0 = smem_addr(smem);
       const uint64_t ad0 = smem_desc_sw128(s0, 16, 1024);
-      const uint64_t bd0 = smem_desc_sw128(s0 + kATileBytes, kBoxBytes, 1024);
-      const uint64_t bd1 = bd0 + ((4 * kBoxBytes) >> 4);
+      uint64_t bd[kBK / 16];
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk) {
+        const int p = (kk * 16) / prow, r0 = kk * 16 - p * prow;
+        bd[kk] = smem_desc_sw128(s0 + kATileBytes + p * part_bytes + r0 * 128, chunk_bytes, 1024);
+      }
+      const uint64_t n1_off = static_cast<uint64_t>((4u * chunk_bytes) >> 4);  // chunk 4 = column 256
       for (int it = 0; it < nk && ok; ++it) {
         const int st = it % S;
         ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
@@ -285,30 +320,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t adesc = ad0 + so + static_cast<uint64_t>(kk * 2);     // + 32 bytes per K step
-          mma_f16(tmem, adesc, bd0 + so + static_cast<uint64_t>(kk * 128), id0, acc);  // + 16 K rows
-          if (N1 > 0) mma_f16(tmem + 256, adesc, bd1 + so + static_cast<uint64_t>(kk * 128), id1, acc);
+          const uint64_t adesc = ad0 + so + static_cast<uint64_t>(kk * 2);  // + 32 bytes per K step
+          mma_f16(tmem, adesc, bd[kk] + so, id0, acc);
+          if (N1 > 0) mma_f16(tmem + 256, adesc, bd[kk] + so + n1_off, id1, acc);
         }
-        mma_commit(&pb->empty[st]);
+        if (CS > 1) mma_commit_mc(&pb->empty[st], mask);
+        else mma_commit(&pb->empty[st]);
       }
       mma_commit(&pb->done);
     }
   } else {
+    // Epilogue: accumulators -> shared memory (the pipeline stages are idle:
+    // every stage, the peers' multicasts included, has been consumed), then
+    // whole rows to global memory with coalesced 16-byte stores.
     ok = mbar_wait(&pb->done, 0, &g_pf_wait_timeouts);
     tc_fence_after();
-    const int lq = warp & 3, row = lq * 32 + lane;
-    const int64_t grow = m0 + row;
+    const int ew = warp - 2, lq = warp & 3, row = lq * 32 + lane;
+    const int NPS = NP + 4;                     // padded row: conflict-free 16-byte writes
     const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16);
+    const float qn = __int_as_float(0x7fc00000);
+    if (kBM * NPS * 4 > S * stage_bytes) {
+      // (too few stages to stage the tile) each thread stores its own row
+      const int64_t grow = m0 + row;
+      for (int c0 = 0; c0 < NTOT; c0 += 16) {
+        float v[16];
+        tmem_ld16(taddr + c0, v);
+        if (grow < a.rows) {
+          float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * NP + c0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = ok ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]) : make_float4(qn, qn, qn, qn);
+        }
+      }
+    } else {
+    fence_proxy_async_smem();
+    float* stg = reinterpret_cast<float*>(smem);
     for (int c0 = 0; c0 < NTOT; c0 += 16) {
       float v[16];
       tmem_ld16(taddr + c0, v);
-      if (grow < a.rows) {
-        float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * NP + c0);
-        const float qn = __int_as_float(0x7fc00000);
+      float4* d4 = reinterpret_cast<float4*>(stg + row * NPS + c0);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          dst[q] = ok ? make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]) : make_float4(qn, qn, qn, qn);
-      }
+      for (int q = 0; q < 4; ++q) d4[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+    named_bar_sync(1, 128);
+    for (int r = ew; r < kBM; r += 4) {
+      const int64_t grow = m0 + r;
+      if (grow >= a.rows) break;
+      const float4* s4 = reinterpret_cast<const float4*>(stg + r * NPS);
+      float4* dst = reinterpret_cast<float4*>(a.part + (static_cast<int64_t>(ks) * a.rows + grow) * NP);
+      for (int c4 = lane; c4 < NP / 4; c4 += 32) dst[c4] = ok ? s4[c4] : make_float4(qn, qn, qn, qn);
+    }
     }
   }
   tc_fence_before();
@@ -317,6 +378,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
+  // no CTA leaves while a peer may still multicast into it or arrive on it
+  if (CS > 1) cluster_sync_all();
 }
 
 // down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
@@ -586,6 +649,22 @@ bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, uint64_t tiles) 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3D map viewing a row-major [outer, inner] 16-bit matrix (inner % 64 == 0)
+// as [inner/64 column chunks][outer rows][64 columns]; box = all chunks of
+// `box_rows` rows, 128-byte swizzle. One copy then lands the chunks one after
+// another in shared memory, each a 128-byte-swizzled MN-major block.
+bool make_chunk_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {64, outer, inner / 64};
+  const cuuint64_t strides[2] = {inner * 2, 128};
+  const cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(inner / 64)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int kSmemBudget = 220 * 1024;
 
 int pick_stages(int stage_bytes) {
@@ -652,8 +731,11 @@ cudaError_t run_prefill(const Problem& p) {
   const unsigned mtiles = static_cast<unsigned>((rows + kBM - 1) / kBM);
   PfDownArgs da;
   const uint64_t hn_tiles = static_cast<uint64_t>(mtiles) * (CH / 64);
-  if (!make_tile_map(&da.tm_a, hn, BF16, hn_tiles) || !make_map(&da.tm_b, p.down_w, BF16, R, CH, 64))
+  // row tiles that share a K slice go in pairs (clusters of 2) once there are two
+  const int cs = mtiles >= 2 ? 2 : 1;
+  if (!make_tile_map(&da.tm_a, hn, BF16, hn_tiles) || !make_chunk_map(&da.tm_b, p.down_w, BF16, R, CH, kBK / cs))
     return cudaErrorInvalidValue;
+  da.cs = cs;
   da.wi = static_cast<const uint16_t*>(p.inject_w);
   da.part = part;
   da.rows = static_cast<int>(rows);
@@ -668,7 +750,8 @@ cudaError_t run_prefill(const Problem& p) {
   const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + wi_stage + sizeof(PipeBars);
   e = ensure_smem<pf_down<BF16>>(dsm);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(pf_down<BF16>, dim3(mtiles, ksplit), dim3(kTcThreads), dsm, p.stream, 1u, da);
+  const unsigned gx = (mtiles + cs - 1) / cs * cs;  // a padded tile loads zeros (out of range) and stores nothing
+  e = launch_pdl(pf_down<BF16>, dim3(gx, ksplit), dim3(kTcThreads), dsm, p.stream, static_cast<unsigned>(cs), da);
   if (e != cudaSuccess) return e;
 
   const int64_t nmid = rows * (R / 4 + C);
