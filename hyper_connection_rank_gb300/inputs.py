@@ -1,4 +1,5 @@
-"""Seeded synthetic inputs for the hyper-connection low-rank mix block.
+"""Seeded synthetic inputs for the hyper-connection low-rank mix block (and the
+row inverse RMS and Engram gate workloads).
 
 This module holds no arithmetic of the block itself: it only draws random
 tensors. Both the oracle-side tests and the GPU benchmark use it, so that the
@@ -37,7 +38,9 @@ M2 = 0x94D049BB133111EB
 MASK64 = (1 << 64) - 1
 
 TENSOR_IDS = {"streams": 1, "prev_out": 2, "prev_gate": 3, "norm_scale": 4,
-              "down_w": 5, "up_w": 6, "inject_w": 7}
+              "down_w": 5, "up_w": 6, "inject_w": 7,
+              # row inverse RMS and Engram gate workloads
+              "x": 8, "key": 9, "query": 10, "value": 11, "key_scale": 12, "query_scale": 13}
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
@@ -109,8 +112,10 @@ def draw(name: str, shape, dtype: str, seed: int = 0, block: int = 0, device="cp
     for s in shape:
         n *= int(s)
     key = stream_key(seed, block, TENSOR_IDS[name])
-    if name in ("streams", "prev_out"):
+    if name in ("streams", "prev_out", "x", "key", "query", "value"):
         x = normal(key, n, device)
+    elif name in ("key_scale", "query_scale"):
+        x = 1.0 + 0.1 * normal(key, n, device)
     elif name == "prev_gate":
         x = uniform(key, n, 0.0, 2.0, device)
     elif name == "norm_scale":
@@ -151,3 +156,19 @@ def make_block(rows: int, C: int, H: int, R: int, dtype: str, seed: int = 0, blo
     d = make_weights(C, H, R, dtype, seed, block, device)
     d.update(make_activations(rows, C, H, dtype, seed, block, prologue, device))
     return d
+
+
+def make_inv_rms_input(rows: int, dim: int, dtype: str, seed: int = 0, device="cpu"):
+    """Hidden state of the row inverse RMS workload (FreeToken PR #101: rows x
+    hc_dim, bf16 in the page's measurements): x ~ N(0, 1)."""
+    return draw("x", (rows, dim), dtype, seed=seed, device=device)
+
+
+def make_engram_inputs(rows: int, M: int, D: int, dtype: str, seed: int = 0, device="cpu"):
+    """Engram gate workload (com.microsoft.EngramGate README): key, query
+    (rows, M, D) ~ N(0, 1); value (rows, D) ~ N(0, 1); per-stream scales (M, D)
+    = 1 + 0.1 N(0, 1). rows = batch * sequence."""
+    kw = dict(dtype=dtype, seed=seed, device=device)
+    return dict(key=draw("key", (rows, M, D), **kw), query=draw("query", (rows, M, D), **kw),
+                value=draw("value", (rows, D), **kw), key_scale=draw("key_scale", (M, D), **kw),
+                query_scale=draw("query_scale", (M, D), **kw))

@@ -1,4 +1,5 @@
-"""CPU oracle of the hyper-connection low-rank mix block -- TEST INFRASTRUCTURE.
+"""CPU oracle of the hyper-connection low-rank mix block, the row inverse RMS
+and the Engram gate -- TEST INFRASTRUCTURE.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package. The GPU library never uses it.
@@ -58,6 +59,11 @@ def lib():
             L.hc_oracle_round.restype = f32
             L.hc_oracle_sigmoid.argtypes = [f32]
             L.hc_oracle_sigmoid.restype = f32
+            f64 = ctypes.c_double
+            L.hc_oracle_inv_rms.argtypes = [vp, i64, i64, f64, ci, vp]
+            L.hc_oracle_inv_rms.restype = ci
+            L.hc_oracle_engram_gate.argtypes = [vp] * 5 + [i64, ci, i64, f64, ci, vp, vp]
+            L.hc_oracle_engram_gate.restype = ci
             L.hc_oracle_to_float.argtypes = [vp, ci, i64, vp]
             L.hc_oracle_from_float.argtypes = [vp, ci, i64, vp]
             _lib = L
@@ -121,6 +127,36 @@ def split_trace(tr, C, H, R):
         out[n] = tr[:, o:o + w]
         o += w
     return out
+
+
+def inv_rms(x, *, dtype, epsilon):
+    """Row inverse RMS of FreeToken PR #101 ("The problem"): float64 array
+    (rows,) of 1/sqrt(mean(x^2) + eps) for x (rows, dim) holding T codes."""
+    x = _as_storage(x, dtype, "x")
+    rows, dim = x.shape
+    out = np.empty(rows, np.float64)
+    if lib().hc_oracle_inv_rms(_ptr(x), rows, dim, float(epsilon), dtype, _ptr(out)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
+
+
+def engram_gate(key, query, value, key_scale, query_scale, *, dtype, epsilon=1e-5):
+    """com.microsoft.EngramGate (its README, "Description"): key, query (rows, M, D),
+    value (rows, D), key_scale, query_scale (M, D), all T codes. Returns
+    (output (rows, M, D) T codes, gate (rows, M) float64)."""
+    key = _as_storage(key, dtype, "key")
+    rows, M, D = key.shape
+    args = [_as_storage(a, dtype, n) for a, n in ((query, "query"), (value, "value"), (key_scale, "key_scale"),
+                                                 (query_scale, "query_scale"))]
+    if args[0].shape != key.shape or args[1].shape != (rows, D) or args[2].shape != (M, D) \
+            or args[3].shape != (M, D):
+        raise ValueError("shape mismatch")
+    out = np.empty(key.shape, _NP_STORAGE[dtype])
+    gate = np.empty((rows, M), np.float64)
+    if lib().hc_oracle_engram_gate(_ptr(key), *[_ptr(a) for a in args], rows, M, D, float(epsilon), dtype,
+                                   _ptr(out), _ptr(gate)) != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out, gate
 
 
 def round_t(x: float, dtype: int) -> float:

@@ -241,7 +241,7 @@ void one_row(const Problem& p, int64_t b, std::vector<float>& scratch) {
 
 extern "C" {
 
-int hc_oracle_abi_version(void) { return 1; }
+int hc_oracle_abi_version(void) { return 2; }
 
 int64_t hc_oracle_trace_floats_per_row(int C, int H, int R) {
   const int64_t CH = static_cast<int64_t>(C) * H;
@@ -279,6 +279,75 @@ int hc_oracle_lowrank_mix(const void* streams, const void* norm_scale, const voi
       for (int64_t b = t; b < rows; b += nt) one_row(p, b, scratch);
     });
   for (auto& th : pool) th.join();
+  return 0;
+}
+
+// ---- Second workload: the row inverse RMS of FreeToken PR #101 ("perf(dsv4):
+// compute the hyper-connection pre-norm in one kernel", sections "The
+// problem" and "Accuracy"): inv[r] = 1 / sqrt(mean_i(x[r, i]^2) + eps), the
+// scalar the hyper-connection pre-norm multiplies into its mix. The page
+// judges a kernel against a float64 evaluation, so that is what this is: the
+// squares and their sequential sum in double, the mean by an IEEE divide, the
+// square root and the reciprocal correctly rounded in double.
+int hc_oracle_inv_rms(const void* x, int64_t rows, int64_t dim, double eps, int dtype, double* out) {
+  if (rows < 0 || dim < 1 || dtype < DT_F32 || dtype > DT_BF16) return 1;
+  if (rows == 0) return 0;
+  if (!x || !out) return 1;
+  for (int64_t r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int64_t i = 0; i < dim; ++i) {
+      const double v = load_t(x, r * dim + i, dtype);
+      ss += v * v;
+    }
+    out[r] = 1.0 / std::sqrt(ss / static_cast<double>(dim) + eps);
+  }
+  return 0;
+}
+
+// ---- Third workload: com.microsoft.EngramGate (its kernel README,
+// "Description", "Inputs", "Outputs", "Attributes"). For every row
+// (batch*sequence index b, stream m) of key and query (rows, M, D):
+//   k^ = key / sqrt(mean(key^2) + eps) * key_norm_scale[m]   (likewise q^)
+//   dot = sum_i k^_i * q^_i / sqrt(D)
+//   gate = sigmoid(sign(dot) * sqrt(max(|dot|, 1e-6)))        (fixed floor)
+//   output[b, m, :] = gate * value[b, :]                       (value shared by the M streams)
+// Evaluated in double (the README fixes float32 accumulation for its kernels;
+// the exact value of the definition is the reference the tests hold a float32
+// kernel to). sign(0) = 0, so a zero dot gives a gate of exactly 0.5. The
+// output is rounded to T through float32 (a double rounding that can move a
+// result by one unit of T only at an exact midpoint). gate_out, if not NULL,
+// receives the double gate of each of the rows * M rows.
+int hc_oracle_engram_gate(const void* key, const void* query, const void* value, const void* key_scale,
+                          const void* query_scale, int64_t rows, int M, int64_t D, double eps, int dtype,
+                          void* output, double* gate_out) {
+  if (rows < 0 || M < 1 || D < 1 || dtype < DT_F32 || dtype > DT_BF16) return 1;
+  if (rows == 0) return 0;
+  if (!key || !query || !value || !key_scale || !query_scale || !output) return 1;
+  for (int64_t b = 0; b < rows; ++b)
+    for (int m = 0; m < M; ++m) {
+      const int64_t row = b * M + m;
+      double ssk = 0.0, ssq = 0.0;
+      for (int64_t i = 0; i < D; ++i) {
+        const double k = load_t(key, row * D + i, dtype), q = load_t(query, row * D + i, dtype);
+        ssk += k * k;
+        ssq += q * q;
+      }
+      const double ik = 1.0 / std::sqrt(ssk / static_cast<double>(D) + eps);
+      const double iq = 1.0 / std::sqrt(ssq / static_cast<double>(D) + eps);
+      double dot = 0.0;
+      for (int64_t i = 0; i < D; ++i) {
+        const double kh = load_t(key, row * D + i, dtype) * ik * load_t(key_scale, m * D + i, dtype);
+        const double qh = load_t(query, row * D + i, dtype) * iq * load_t(query_scale, m * D + i, dtype);
+        dot += kh * qh;
+      }
+      dot /= std::sqrt(static_cast<double>(D));
+      const double sgn = dot > 0.0 ? 1.0 : (dot < 0.0 ? -1.0 : 0.0);
+      const double z = sgn * std::sqrt(std::max(std::fabs(dot), 1e-6));
+      const double g = 1.0 / (1.0 + std::exp(-z));
+      if (gate_out) gate_out[row] = g;
+      for (int64_t i = 0; i < D; ++i)
+        store_t(output, row * D + i, static_cast<float>(g * load_t(value, b * D + i, dtype)), dtype);
+    }
   return 0;
 }
 

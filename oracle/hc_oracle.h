@@ -36,6 +36,15 @@ int hc_oracle_lowrank_mix(const void* streams, const void* norm_scale, const voi
                           float epsilon, float reduction_scale, float silu_alpha, float gate_div,
                           float gate_mul, int dtype, void* pre_output, void* post_gate,
                           void* streams_out, float* trace, int nthreads);
+/* Row inverse RMS (FreeToken PR #101): out[r] = 1/sqrt(mean_i(x[r,i]^2) + eps)
+ * in double, for x (rows, dim) of type dtype. Returns 0, or 1 on a bad argument. */
+int hc_oracle_inv_rms(const void* x, int64_t rows, int64_t dim, double eps, int dtype, double* out);
+/* com.microsoft.EngramGate: key, query (rows, M, D); value (rows, D); key_scale,
+ * query_scale (M, D); output (rows, M, D), all of type dtype; gate_out (rows*M)
+ * doubles or NULL. Evaluated in double, output rounded to T. */
+int hc_oracle_engram_gate(const void* key, const void* query, const void* value, const void* key_scale,
+                          const void* query_scale, int64_t rows, int M, int64_t D, double eps, int dtype,
+                          void* output, double* gate_out);
 /* The oracle's own rounding to T (identity for float32) and sigmoid, exposed
  * so the tests can pin them against independent library conversions. */
 float hc_oracle_round(float x, int dtype);
