@@ -27,7 +27,8 @@ DTYPE_CODES = {torch.float32: HC_F32, torch.float16: HC_F16, torch.bfloat16: HC_
 
 # Every symbol include/hc_lowrank_mix.h declares.
 EXPORTS = ("hc_attrs_default", "hc_lowrank_mix_path", "hc_lowrank_mix_workspace_size", "hc_lowrank_mix",
-           "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts", "hc_debug_sigmoid_exact")
+           "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts", "hc_debug_sigmoid_exact",
+           "hc_inv_rms", "hc_engram_gate")
 
 
 class HcAttrs(ctypes.Structure):
@@ -69,6 +70,11 @@ def load_library(path: str = LIB_PATH):
         L.hc_debug_wait_timeouts.restype = ctypes.c_uint
         L.hc_debug_sigmoid_exact.argtypes = [ci, vp, vp, vp]
         L.hc_debug_sigmoid_exact.restype = ci
+        f32 = ctypes.c_float
+        L.hc_inv_rms.argtypes = [vp, i64, i64, f32, ci, vp, vp]
+        L.hc_inv_rms.restype = ci
+        L.hc_engram_gate.argtypes = [vp] * 5 + [i64, ci, i64, f32, ci, vp, vp]
+        L.hc_engram_gate.restype = ci
         _lib = L
         return L
 
@@ -177,3 +183,49 @@ def debug_sigmoid_exact(dt: torch.dtype, device="cuda"):
     s = torch.cuda.current_stream(fast.device)
     check(lib().hc_debug_sigmoid_exact(DTYPE_CODES[dt], _ptr(fast), _ptr(acc), s.cuda_stream))
     return fast, acc
+
+
+def _check_cuda(name, t, dt):
+    if not t.is_cuda or t.dtype != dt or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of dtype {dt}")
+
+
+def inv_rms(x, epsilon=1e-6, *, out=None, stream=None):
+    """Row inverse RMS (hc_inv_rms): 1/sqrt(mean(x^2, -1) + epsilon) as float32,
+    shape x.shape[:-1]. x: contiguous CUDA tensor (float32, float16 or bfloat16)."""
+    dt = x.dtype
+    if dt not in DTYPE_CODES:
+        raise TypeError(f"unsupported dtype {dt}")
+    _check_cuda("x", x, dt)
+    dim = x.shape[-1]
+    rows = x.numel() // max(dim, 1)
+    if out is None:
+        out = torch.empty(x.shape[:-1], dtype=torch.float32, device=x.device)
+    s = torch.cuda.current_stream(x.device) if stream is None else stream
+    check(lib().hc_inv_rms(_ptr(x), rows, dim, float(epsilon), DTYPE_CODES[dt], _ptr(out), s.cuda_stream))
+    return out
+
+
+def engram_gate(key, query, value, key_norm_scale, query_norm_scale, epsilon=1e-5, *, out=None, stream=None):
+    """com.microsoft.EngramGate (hc_engram_gate). key, query: (B, S, M, D);
+    value: (B, S, D); scales: (M, D); all one dtype on the GPU. Returns the gated
+    value (B, S, M, D)."""
+    dt = key.dtype
+    if dt not in DTYPE_CODES:
+        raise TypeError(f"unsupported dtype {dt}")
+    for n, t in (("key", key), ("query", query), ("value", value), ("key_norm_scale", key_norm_scale),
+                 ("query_norm_scale", query_norm_scale)):
+        _check_cuda(n, t, dt)
+    if key.dim() < 2 or query.shape != key.shape:
+        raise ValueError("query must have the shape of key (..., M, D)")
+    M, D = key.shape[-2], key.shape[-1]
+    rows = key.numel() // max(M * D, 1)
+    if tuple(value.shape) != tuple(key.shape[:-2]) + (D,) or tuple(key_norm_scale.shape) != (M, D) \
+            or tuple(query_norm_scale.shape) != (M, D):
+        raise ValueError("value must be (..., D) and the scales (M, D)")
+    if out is None:
+        out = torch.empty_like(key)
+    s = torch.cuda.current_stream(key.device) if stream is None else stream
+    check(lib().hc_engram_gate(_ptr(key), _ptr(query), _ptr(value), _ptr(key_norm_scale), _ptr(query_norm_scale),
+                               rows, M, D, float(epsilon), DTYPE_CODES[dt], _ptr(out), s.cuda_stream))
+    return out

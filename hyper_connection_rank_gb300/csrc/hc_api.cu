@@ -14,6 +14,7 @@
 #include <cstring>
 
 #include "hc_internal.h"
+#include "hc_row_ops.h"
 
 namespace {
 
@@ -236,6 +237,70 @@ hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_o
   const cudaError_t e = hc::launch_sigmoid_codes(dtype, static_cast<uint16_t*>(fast_out), static_cast<uint16_t*>(acc_out),
                                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return hc::set_error(HC_ERR_CUDA, cudaGetErrorString(e));
+  return HC_OK;
+}
+
+
+// ---------------------------------------------------------------------------
+// Row inverse RMS (FreeToken PR #101) and com.microsoft.EngramGate: declared
+// in include/hc_row_ops.h.
+
+hc_status_t hc_inv_rms(const void* x, int64_t rows, int64_t dim, float epsilon, hc_dtype_t dtype, float* out,
+                       cudaStream_t stream) {
+  if (!dtype_valid(dtype)) return fail(HC_ERR_INVALID_ARG, "invalid dtype %d", static_cast<int>(dtype));
+  if (rows < 0 || dim < 1) return fail(HC_ERR_INVALID_ARG, "invalid sizes rows=%lld dim=%lld",
+                                       static_cast<long long>(rows), static_cast<long long>(dim));
+  if (rows >= (int64_t{1} << 31) || rows * dim > (int64_t{1} << 40))
+    return fail(HC_ERR_UNSUPPORTED, "sizes beyond the library's limits");
+  if (rows == 0) return HC_OK;
+  if (x == nullptr || out == nullptr) return fail(HC_ERR_INVALID_ARG, "null pointer");
+  const uintptr_t xs = reinterpret_cast<uintptr_t>(x), os = reinterpret_cast<uintptr_t>(out);
+  const Span in{"x", xs, xs + static_cast<uintptr_t>(rows * dim) * hc::dtype_size(dtype)};
+  const Span o{"out", os, os + static_cast<uintptr_t>(rows) * 4u};
+  if (overlaps(in, o)) return fail(HC_ERR_INVALID_ARG, "out overlaps x");
+  int num_sms = 0;
+  hc_status_t st = device_info(&num_sms);
+  if (st != HC_OK) return st;
+  const bool vec = aligned16(x) && (dim * static_cast<int64_t>(hc::dtype_size(dtype))) % 16 == 0;
+  const cudaError_t e = hc::launch_inv_rms(x, rows, dim, epsilon, dtype, out, vec, stream);
+  if (e != cudaSuccess) return fail(HC_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return HC_OK;
+}
+
+hc_status_t hc_engram_gate(const void* key, const void* query, const void* value, const void* key_norm_scale,
+                           const void* query_norm_scale, int64_t rows, int hc_mult, int64_t hidden, float epsilon,
+                           hc_dtype_t dtype, void* output, cudaStream_t stream) {
+  if (!dtype_valid(dtype)) return fail(HC_ERR_INVALID_ARG, "invalid dtype %d", static_cast<int>(dtype));
+  if (rows < 0 || hc_mult < 1 || hidden < 1)
+    return fail(HC_ERR_INVALID_ARG, "invalid sizes rows=%lld hc_mult=%d hidden=%lld", static_cast<long long>(rows),
+                hc_mult, static_cast<long long>(hidden));
+  if (rows * hc_mult >= (int64_t{1} << 31) || rows * hc_mult * hidden > (int64_t{1} << 40))
+    return fail(HC_ERR_UNSUPPORTED, "sizes beyond the library's limits");
+  if (rows == 0) return HC_OK;
+  if (!key || !query || !value || !key_norm_scale || !query_norm_scale || !output)
+    return fail(HC_ERR_INVALID_ARG, "null pointer");
+  const size_t es = hc::dtype_size(dtype);
+  auto span = [](const char* n, const void* p, size_t bytes) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Span{n, a, a + bytes};
+  };
+  const size_t row_bytes = static_cast<size_t>(rows) * hc_mult * hidden * es;
+  const Span ins[5] = {span("key", key, row_bytes), span("query", query, row_bytes),
+                       span("value", value, static_cast<size_t>(rows) * hidden * es),
+                       span("key_norm_scale", key_norm_scale, static_cast<size_t>(hc_mult) * hidden * es),
+                       span("query_norm_scale", query_norm_scale, static_cast<size_t>(hc_mult) * hidden * es)};
+  const Span o = span("output", output, row_bytes);
+  for (const Span& in : ins)
+    if (overlaps(o, in)) return fail(HC_ERR_INVALID_ARG, "output overlaps input %s", in.name);
+  int num_sms = 0;
+  hc_status_t st = device_info(&num_sms);
+  if (st != HC_OK) return st;
+  hc::EngramProblem p{key, query, value, key_norm_scale, query_norm_scale, rows, hc_mult, hidden, epsilon, dtype,
+                      output, false, stream};
+  p.vec = (hidden * static_cast<int64_t>(es)) % 16 == 0 && aligned16(key) && aligned16(query) && aligned16(value) &&
+          aligned16(key_norm_scale) && aligned16(query_norm_scale) && aligned16(output);
+  const cudaError_t e = hc::launch_engram_gate(p);
+  if (e != cudaSuccess) return fail(HC_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
   return HC_OK;
 }
 
