@@ -376,8 +376,8 @@ def cpu_baseline(seconds):
 def sweep(hc, I, dev, pk):
     """Other configurations of the metric (context lines, not the headline):
     decode rows 1/2/4/8 in bf16 and fp16 (96-block graphs; us/block also as the
-    slope between 96- and 48-block graphs, min over 15 x 10 replays), and the
-    8192-row prefill blocks."""
+    slope between 96- and 48-block graphs, min over 15 x 10 replays), the
+    8192-row prefill blocks, and the two companion row operations."""
     import torch
     out = {}
     flags = hc.HC_FLAG_WEIGHTS_STATIC
@@ -444,27 +444,102 @@ def sweep(hc, I, dev, pk):
             hc.lowrank_mix(d["streams"], d["norm_scale"], d["down_w"], d["up_w"], d["inject_w"], d["prev_out"],
                            d["prev_gate"], num_branches=Cp, out=(pre, post, sout), workspace=ws, **QWEN)
 
-        for _ in range(3):
-            call()
-        torch.cuda.synchronize()
-        ts = []
-        for _ in range(10):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            call()
-            e1.record()
-            e1.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        t = min(ts) / 1000
+        # four back-to-back blocks per graph replay (inputs far larger than L2)
+        tmin, tmed = graph_time([call] * 4, reps=10)
+        t = tmin * 1e-6
         b, f = block_bytes(rows, Cp, Hp, R, 2), block_flops(rows, Cp, Hp, R)
         t_roof = max(b / (pk["hbm"] * 1e9), f / (pk["bf16"] * 1e12))
         out[f"prefill_rows{rows}_C{Cp}_H{Hp}_{dt}"] = {
             "path": hc.PATH_NAMES[hc.path(rows, Cp, Hp, R, tdt)],
-            "us_per_block": round(1e6 * t, 2), "us_per_block_median": round(1e3 * statistics.median(ts), 2),
+            "us_per_block": round(1e6 * t, 2), "us_per_block_median": round(tmed, 2),
             "rows_per_s": round(rows / t, 1), "hbm_frac": round(b / t / 1e9 / pk["hbm"], 4),
             "tensor_frac": round(f / t / 1e12 / pk["bf16"], 4), "roofline_frac": round(t_roof / t, 4)}
         del d
         torch.cuda.empty_cache()
+    out.update(sweep_row_ops(hc, I, dev, pk))
+    return out
+
+
+def graph_time(calls, reps=15):
+    """Device time (us) per call of the list `calls`, captured once into a CUDA
+    graph and replayed: min and median over `reps` replays, so no host-side
+    launch overhead enters the figure."""
+    import torch
+    dev = torch.cuda.current_device()
+    for c in calls[:3]:
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for c in calls:
+                c()
+    torch.cuda.current_stream(dev).wait_stream(s)
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        e1.synchronize()
+        ts.append(1000 * e0.elapsed_time(e1) / len(calls))
+    del g
+    return min(ts), statistics.median(ts)
+
+
+def timed_rotating(make, call, bytes_each, target=400 << 20, max_calls=64):
+    """Device time (us) per call of call(inputs), the calls cycling through
+    enough copies of the inputs (made by `make`) to span `target` bytes (about
+    three L2s): each call reads data the previous ones evicted, and no flush
+    leaves dirty lines to be written back during a timed call. Timed as one
+    CUDA graph of the calls (graph_time)."""
+    ncopy = max(1, -(-target // bytes_each))
+    copies = [make(i) for i in range(ncopy)]
+    n = max(ncopy, min(max_calls, 4 * ncopy))
+    tmin, tmed = graph_time([(lambda a=copies[i % ncopy]: call(a)) for i in range(n)])
+    del copies
+    return tmin, tmed
+
+
+def sweep_row_ops(hc, I, dev, pk):
+    """The two companion row operations, each call on inputs not in L2 (the
+    calls cycle through copies spanning about three L2s): the row inverse RMS
+    at the shapes FreeToken PR #101 measures (hc_dim 16384, 64 to 8192 rows,
+    bf16) and the Engram gate at 8192 tokens x hc_mult 4 x hidden 4096 (fp16).
+    Bytes = what each must read and write once."""
+    import torch
+    out = {}
+    for rows in (64, 512, 4096, 8192):
+        dim = 16384
+        b = rows * dim * 2 + rows * 4
+
+        def make(i, rows=rows, dim=dim):
+            return (I.make_inv_rms_input(rows, dim, "bf16", seed=i, device=dev),
+                    torch.empty(rows, dtype=torch.float32, device=dev))
+
+        tmin, tmed = timed_rotating(make, lambda a: hc.inv_rms(a[0], 1e-6, out=a[1]), b)
+        out[f"inv_rms_rows{rows}_dim{dim}_bf16"] = {
+            "us": round(tmin, 2), "us_median": round(tmed, 2), "bytes": b,
+            "GB_s": round(b / (tmin * 1e-6) / 1e9, 1), "hbm_frac": round(b / (tmin * 1e-6) / 1e9 / pk["hbm"], 4)}
+        torch.cuda.empty_cache()
+    rows, M, D = 8192, 4, 4096
+    b = (3 * rows * M * D + rows * D + 2 * M * D) * 2
+
+    def make_e(i):
+        d = I.make_engram_inputs(rows, M, D, "f16", seed=i, device=dev)
+        d["out"] = torch.empty_like(d["key"])
+        return d
+
+    tmin, tmed = timed_rotating(make_e, lambda d: hc.engram_gate(d["key"], d["query"], d["value"], d["key_scale"],
+                                                                 d["query_scale"], 1e-5, out=d["out"]), b)
+    out[f"engram_gate_rows{rows}_M{M}_D{D}_f16"] = {
+        "us": round(tmin, 2), "us_median": round(tmed, 2), "bytes": b,
+        "GB_s": round(b / (tmin * 1e-6) / 1e9, 1), "hbm_frac": round(b / (tmin * 1e-6) / 1e9 / pk["hbm"], 4)}
+    torch.cuda.empty_cache()
     return out
 
 

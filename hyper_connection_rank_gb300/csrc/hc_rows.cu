@@ -86,6 +86,22 @@ __device__ __forceinline__ void group_sum(float (&v)[NV], float (*red)[kRowThrea
   }
 }
 
+// out[0 .. VE) = T(gate * value vector u)
+template <typename T> __device__ __forceinline__ void store_gated(T* dst, const uint4& u, float gate) {
+  constexpr int VE = Vec16<T>::N;
+  float f[VE];
+  Vec16<T>::unpack(u, f);
+  if constexpr (VE == 8) {
+    float o[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(gate, f[e]);
+    st16(dst, V8<T>::pack(o));
+  } else {
+    st16(dst, make_uint4(__float_as_uint(__fmul_rn(gate, f[0])), __float_as_uint(__fmul_rn(gate, f[1])),
+                         __float_as_uint(__fmul_rn(gate, f[2])), __float_as_uint(__fmul_rn(gate, f[3]))));
+  }
+}
+
 // ---------------------------------------------------------------- inv_rms --
 
 template <typename T, int G>
@@ -132,6 +148,10 @@ __global__ void __launch_bounds__(kRowThreads) inv_rms_kernel(const T* __restric
 
 // ------------------------------------------------------------ engram_gate --
 
+// Every load a row needs is issued before any is used: U vectors each of
+// key, query, the two scale rows and the value row per thread and round, so
+// a row costs one memory round trip (the value vectors of the first round
+// stay in registers for the output pass; longer rows load the rest again).
 template <typename T, int G>
 __global__ void __launch_bounds__(kRowThreads)
 engram_gate_kernel(const T* __restrict__ key, const T* __restrict__ query, const T* __restrict__ value,
@@ -139,13 +159,16 @@ engram_gate_kernel(const T* __restrict__ key, const T* __restrict__ query, const
                    float eps, T* __restrict__ out, int vec) {
   __shared__ float red[3][kRowThreads / 32];
   constexpr int VE = Vec16<T>::N;
-  constexpr int U = kRowUnroll / 2;  // key and query vectors in flight per thread: 2 x U
+  constexpr int U = 2;  // vectors per tensor per thread and round
   const int t = threadIdx.x % G;
   const int64_t rr = static_cast<int64_t>(blockIdx.x) * (kRowThreads / G) + threadIdx.x / G;
   const bool live = rr < nrows;
   const int64_t b = live ? rr / M : 0;
   const int m = live ? static_cast<int>(rr - b * M) : 0;
+  const T* vr = value + b * D;
   float acc[3] = {0.0f, 0.0f, 0.0f};  // sum key^2, sum query^2, sum (key ks)(query qs)
+  uint4 held[U];                      // value vectors of the first round
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
   if (live) {
     const T* kr = key + rr * D;
     const T* qr = query + rr * D;
@@ -154,37 +177,38 @@ engram_gate_kernel(const T* __restrict__ key, const T* __restrict__ query, const
     if (vec) {
       const int64_t nv = D / VE;
       for (int64_t v0 = t; v0 < nv; v0 += U * G) {
-        uint4 uk[U], uq[U];
+        uint4 uk[U], uq[U], zk[U], zq[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
           const int64_t v = v0 + j * G;
-          uk[j] = v < nv ? ld16(kr + v * VE) : make_uint4(0u, 0u, 0u, 0u);
-          uq[j] = v < nv ? ld16(qr + v * VE) : make_uint4(0u, 0u, 0u, 0u);
+          const bool in = v < nv;
+          uk[j] = in ? ld16(kr + v * VE) : z4;
+          uq[j] = in ? ld16(qr + v * VE) : z4;
+          zk[j] = in ? ld16(ksr + v * VE) : z4;
+          zq[j] = in ? ld16(qsr + v * VE) : z4;
+          if (v0 == t) held[j] = in ? ld16(vr + v * VE) : z4;
         }
         float pk[U], pq[U], pc[U];
 #pragma unroll
         for (int j = 0; j < U; ++j) {
-          const int64_t v = v0 + j * G;
           float fk[VE], fq[VE], sk[VE], sq[VE];
           Vec16<T>::unpack(uk[j], fk);
           Vec16<T>::unpack(uq[j], fq);
-          const uint4 zk = v < nv ? ld16(ksr + v * VE) : make_uint4(0u, 0u, 0u, 0u);
-          const uint4 zq = v < nv ? ld16(qsr + v * VE) : make_uint4(0u, 0u, 0u, 0u);
-          Vec16<T>::unpack(zk, sk);
-          Vec16<T>::unpack(zq, sq);
+          Vec16<T>::unpack(zk[j], sk);
+          Vec16<T>::unpack(zq[j], sq);
           pk[j] = sumsq<VE>(fk);
           pq[j] = sumsq<VE>(fq);
           float c[VE];
 #pragma unroll
           for (int e = 0; e < VE; ++e) c[e] = __fmul_rn(__fmul_rn(fk[e], sk[e]), __fmul_rn(fq[e], sq[e]));
-          float s = __fadd_rn(c[0], c[1]);
+          float sacc = __fadd_rn(c[0], c[1]);
 #pragma unroll
-          for (int e = 2; e < VE; e += 2) s = __fadd_rn(s, __fadd_rn(c[e], c[e + 1]));
-          pc[j] = s;
+          for (int e = 2; e < VE; e += 2) sacc = __fadd_rn(sacc, __fadd_rn(c[e], c[e + 1]));
+          pc[j] = sacc;
         }
-        acc[0] = __fadd_rn(acc[0], __fadd_rn(__fadd_rn(pk[0], pk[1]), __fadd_rn(pk[2], pk[3])));
-        acc[1] = __fadd_rn(acc[1], __fadd_rn(__fadd_rn(pq[0], pq[1]), __fadd_rn(pq[2], pq[3])));
-        acc[2] = __fadd_rn(acc[2], __fadd_rn(__fadd_rn(pc[0], pc[1]), __fadd_rn(pc[2], pc[3])));
+        acc[0] = __fadd_rn(acc[0], __fadd_rn(pk[0], pk[1]));
+        acc[1] = __fadd_rn(acc[1], __fadd_rn(pq[0], pq[1]));
+        acc[2] = __fadd_rn(acc[2], __fadd_rn(pc[0], pc[1]));
       }
     } else {
       for (int64_t i = t; i < D; i += G) {
@@ -205,23 +229,15 @@ engram_gate_kernel(const T* __restrict__ key, const T* __restrict__ query, const
   const float sgn = dot > 0.0f ? 1.0f : (dot < 0.0f ? -1.0f : 0.0f);
   const float z = __fmul_rn(sgn, __fsqrt_rn(fmaxf(fabsf(dot), 1e-6f)));
   const float gate = sigmoid_acc(z);
-  const T* vr = value + b * D;
   T* orow = out + rr * D;
   if (vec) {
     const int64_t nv = D / VE;
-    for (int64_t v = t; v < nv; v += G) {
-      float f[VE];
-      Vec16<T>::unpack(ld16(vr + v * VE), f);
-      if constexpr (VE == 8) {
-        float o[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) o[e] = __fmul_rn(gate, f[e]);
-        st16(orow + v * VE, V8<T>::pack(o));
-      } else {
-        st16(orow + v * VE, make_uint4(__float_as_uint(__fmul_rn(gate, f[0])), __float_as_uint(__fmul_rn(gate, f[1])),
-                                       __float_as_uint(__fmul_rn(gate, f[2])), __float_as_uint(__fmul_rn(gate, f[3]))));
-      }
+    for (int j = 0; j < U; ++j) {
+      const int64_t v = t + j * G;
+      if (v < nv) store_gated<T>(orow + v * VE, held[j], gate);
     }
+    for (int64_t v = t + U * G; v < nv; v += G) store_gated<T>(orow + v * VE, ld16(vr + v * VE), gate);
   } else {
     for (int64_t i = t; i < D; i += G) stf(orow + i, __fmul_rn(gate, ldf(vr + i)));
   }
