@@ -164,6 +164,8 @@ def run_ours(args, rank, world, local_rank):
 
     if args.profile_case == "prefill":
         return profile_prefill(args, hc, I, dev)
+    if args.profile_case == "rowops":
+        return profile_rowops(args, hc, I, dev)
     rows = args.rows
     flags = hc.HC_FLAG_WEIGHTS_STATIC
     assert hc.path(rows, C, H, R, torch.bfloat16, flags) == hc.HC_PATH_DECODE
@@ -283,6 +285,23 @@ def profile_prefill(args, hc, I, dev):
                        d["prev_gate"], num_branches=C, out=out, workspace=ws, **QWEN)
     torch.cuda.synchronize()
     return {"profile_case": f"prefill rows={rows} bf16, {args.warmup}+{args.steps} eager blocks"}
+
+
+def profile_rowops(args, hc, I, dev):
+    """Profiler case for the two row operations: the row inverse RMS on 8192 x
+    16384 bf16 (268 MB) and the Engram gate on 8192 x 4 x 4096 fp16 (872 MB),
+    warmup + steps eager calls each, alternating."""
+    import torch
+    x = I.make_inv_rms_input(8192, 16384, "bf16", seed=0, device=dev)
+    o = torch.empty(8192, dtype=torch.float32, device=dev)
+    d = I.make_engram_inputs(8192, 4, 4096, "f16", seed=0, device=dev)
+    eo = torch.empty_like(d["key"])
+    for _ in range(args.warmup + args.steps):
+        hc.inv_rms(x, 1e-6, out=o)
+        hc.engram_gate(d["key"], d["query"], d["value"], d["key_scale"], d["query_scale"], 1e-5, out=eo)
+    torch.cuda.synchronize()
+    return {"profile_case": f"row ops (inv_rms 8192x16384 bf16, engram 8192x4x4096 f16), "
+                            f"{args.warmup}+{args.steps} eager calls each"}
 
 
 def e2e_measure(args, hc, I, weights, dev, flags):
@@ -602,7 +621,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--rows", type=int, default=1, help="decode rows per block (1..8)")
-    ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "prefill"),
+    ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "prefill", "rowops"),
                     help="small eager case for profiler captures (not a benchmark result)")
     args = ap.parse_args()
     if args.warmup < 3:
