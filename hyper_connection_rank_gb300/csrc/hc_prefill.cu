@@ -420,17 +420,42 @@ __global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, in
 // Persistent up projection. A tile is 128 rows x 64 features; its C branches
 // are processed in groups of (up to) four, one group per unit of work, so an
 // accumulator is at most 4 x 64 = 256 tensor-memory columns and two of them
-// (double buffering) always fit. The epilogue keeps the pre-mix sum of a tile
-// in registers across its groups, adding branches in order 0..C-1. The hn
-// values the epilogue needs come into shared memory by TMA (128-byte swizzle,
-// double-buffered per unit), so no global load sits on the epilogue's path.
+// (double buffering) always fit. CTA i takes tiles i, i + grid, ..., so the
+// CTAs at work at any moment cover a few neighbouring row tiles (their hn
+// reads and pre_output writes stay close). Per unit and K block a stage holds
+// the d box (128 rows x 64) and, by one 3D copy, the group's W_u columns (a
+// view of W_u as [branches][R rows][H columns], box {64, 64, branches}). The
+// hn boxes of a unit arrive one branch at a time into a ring of slots, in the
+// order the epilogue consumes them, issued by a warp of their own so that they
+// run ahead of the epilogue independently of the operand stages. (Keeping a
+// row tile's d resident and walking that row tile's feature tiles read fewer
+// bytes but spread the concurrent CTAs over all row tiles, and measured slower.)
+// The epilogue keeps the pre-mix sum of a tile in registers across its
+// groups, adding branches in order 0..C-1. Warps: 0 loads d and W_u, 1 issues
+// the MMAs and owns the tensor memory, 2..17 run the epilogue, 18 loads hn.
+//
+// g = rT(sigmoid(u)) for u = rT(up): in bf16 it is read from a table of the
+// accurate sigmoid over every bf16 u whose result is not a constant
+// (|u| in [2^-9, 8) for u >= 0, [2^-9, 96] for u < 0; below, g = 1/2; above,
+// g = 1 resp. 0; NaN stays NaN), built by the CTA at start: bit for bit the
+// accurate rounded sigmoid, with neither MUFU operation of the formula. fp16
+// keeps the branch-free fast sigmoid (its rounding can differ in one ulp near
+// a rounding midpoint).
 constexpr int kUpEpiWarps = 16;
-constexpr int kUpThreads = 64 + 32 * kUpEpiWarps;
+constexpr int kUpHnWarp = 2 + kUpEpiWarps;                 // the warp that loads hn
+constexpr int kUpThreads = 32 * (kUpHnWarp + 1);
 constexpr int kHnBoxBytes = 128 * 64 * 2;   // one branch: 128 rows x 64 features
 constexpr int kUpStages = 2;
+constexpr int kHnSlotsMax = 6;
+constexpr uint32_t kSigLo = 0x3AFFu;        // largest bf16 magnitude code below 2^-9
+constexpr uint32_t kSigPosHi = 0x4100u;     // 8.0
+constexpr uint32_t kSigNegHi = 0x42C0u;     // 96.0
+constexpr int kSigPosN = static_cast<int>(kSigPosHi - kSigLo + 1);
+constexpr int kSigN = kSigPosN + static_cast<int>(kSigNegHi - kSigLo + 1);
+constexpr int kSigBytes = (kSigN * 2 + 127) / 128 * 128;
 
 struct UpBars {
-  uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[2], hne[2];
+  uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[kHnSlotsMax], hne[kHnSlotsMax];
   uint32_t tmem_base;
 };
 
@@ -441,20 +466,43 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   return c;
 }
 
+__device__ __forceinline__ uint32_t bf16_code(float x) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
+}
+
+// g for the bf16 code c of u, from the table (see above).
+__device__ __forceinline__ float sig_table(const uint16_t* tab, uint32_t c) {
+  const uint32_t mag = c & 0x7FFFu, neg = c >> 15;
+  const uint32_t hi = neg ? kSigNegHi : kSigPosHi;
+  const uint32_t m2 = min(max(mag, kSigLo), hi);
+  const uint32_t idx = m2 - kSigLo + (neg ? static_cast<uint32_t>(kSigPosN) : 0u);
+  const uint32_t g = mag > 0x7F80u ? 0x7FC0u : static_cast<uint32_t>(tab[idx]);
+  return __uint_as_float(g << 16);
+}
+
 template <typename T, bool BF16>
 __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ PfUpArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int C = a.C, H = a.H, R = a.R;
-  const int G = (C + 3) / 4, GC = C < 4 ? C : 4;       // groups per tile, branches per group
-  const int stage_bytes = kATileBytes + GC * kBoxBytes;
-  uint8_t* hn_s = smem + kUpStages * stage_bytes;       // [2 buffers][GC][128 rows][64] (swizzled)
-  UpBars* pb = reinterpret_cast<UpBars*>(hn_s + 2 * GC * kHnBoxBytes);
-  const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
+  const int C = a.C, H = a.H, R = a.R, NH = a.nbuf;
+  const int G = (C + 3) / 4, GC = C < 4 ? C : 4;        // groups per tile, branches per group
   const int nk = R / kBK, NG = 64 * GC;
+  const int stage_bytes = kATileBytes + GC * kBoxBytes;  // d box, then W_u of one K block for the group
+  uint8_t* st_s = smem;                                  // [kUpStages][d box | GC][...]
+  uint8_t* hn_s = st_s + kUpStages * stage_bytes;        // [NH][128 rows][64] (swizzled)
+  uint16_t* sig = reinterpret_cast<uint16_t*>(hn_s + NH * kHnBoxBytes);
+  UpBars* pb = reinterpret_cast<UpBars*>(reinterpret_cast<uint8_t*>(sig) + kSigBytes);
+  const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
   const uint32_t ncols = tmem_cols_for(2 * NG);
 
+  if (BF16) {
+    // the table: code of rT(sigmoid_acc(u)) for every u it covers
+    for (int i = threadIdx.x; i < kSigN; i += blockDim.x) {
+      const uint32_t c = i < kSigPosN ? kSigLo + i : 0x8000u | (kSigLo + (i - kSigPosN));
+      sig[i] = static_cast<uint16_t>(bf16_code(sigmoid_acc(__uint_as_float(c << 16))));
+    }
+  }
   if (warp == 0 && lane == 0) {
     for (int st = 0; st < kUpStages; ++st) {
       mbar_init(&pb->full[st], 1);
@@ -463,8 +511,10 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     for (int b = 0; b < 2; ++b) {
       mbar_init(&pb->accf[b], 1);
       mbar_init(&pb->acce[b], kUpEpiWarps);
-      mbar_init(&pb->hnf[b], 1);
-      mbar_init(&pb->hne[b], kUpEpiWarps);
+    }
+    for (int q = 0; q < NH; ++q) {
+      mbar_init(&pb->hnf[q], 1);
+      mbar_init(&pb->hne[q], kUpEpiWarps);
     }
     fence_mbar_init();
     tma_prefetch_desc(&a.tm_a);
@@ -484,27 +534,39 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
 
   if (warp == 0) {
     if (lane == 0) {
-      int it = 0, unit = 0;
+      int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
-        for (int g = 0; g < G && ok; ++g, ++unit) {
-          const int buf = unit & 1, use = unit >> 1, c_lo = g * 4, nc = min(4, C - c_lo);
-          ok = mbar_wait(&pb->hne[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
-          if (!ok) break;
-          mbar_arrive_expect_tx(&pb->hnf[buf], static_cast<uint32_t>(nc * kHnBoxBytes));
-          for (int cc = 0; cc < nc; ++cc)
-            tma_load_3d(hn_s + (buf * GC + cc) * kHnBoxBytes, &a.tm_hn, 0, 0,
-                        (m0 / kBM) * (C * H / 64) + ((c_lo + cc) * H + h0) / 64, &pb->hnf[buf]);
+        for (int g = 0; g < G && ok; ++g) {
+          const int c_lo = g * 4, nc = min(4, C - c_lo);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int st = it % kUpStages;
             ok = mbar_wait(&pb->empty[st], ((it / kUpStages) & 1) ^ 1, &g_pf_wait_timeouts);
             if (!ok) break;
-            uint8_t* sp = smem + st * stage_bytes;
+            uint8_t* sp = st_s + st * stage_bytes;
             mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + nc * kBoxBytes));
             tma_load_2d(sp, &a.tm_a, kb * kBK, m0, &pb->full[st]);
-            for (int cc = 0; cc < nc; ++cc)
-              tma_load_2d(sp + kATileBytes + cc * kBoxBytes, &a.tm_b, (c_lo + cc) * H + h0, kb * kBK, &pb->full[st]);
+            tma_load_3d(sp + kATileBytes, &a.tm_b, h0, kb * kBK, c_lo, &pb->full[st]);
+          }
+        }
+      }
+    }
+  } else if (warp == kUpHnWarp) {
+    if (lane == 0) {
+      int hseq = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int mt = tile / n_h, h0 = (tile % n_h) * 64;
+        for (int g = 0; g < G && ok; ++g) {
+          const int c_lo = g * 4, nc = min(4, C - c_lo);
+          for (int cc = 0; cc < nc && ok; ++cc, ++hseq) {
+            const int q = hseq % NH;
+            ok = mbar_wait(&pb->hne[q], ((hseq / NH) & 1) ^ 1, &g_pf_wait_timeouts);
+            if (!ok) break;
+            mbar_arrive_expect_tx(&pb->hnf[q], static_cast<uint32_t>(kHnBoxBytes));
+            tma_load_3d(hn_s + q * kHnBoxBytes, &a.tm_hn, 0, 0, mt * (C * H / 64) + ((c_lo + cc) * H + h0) / 64,
+                        &pb->hnf[q]);
           }
         }
       }
@@ -513,17 +575,17 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     if (lane == 0) {
       int it = 0, unit = 0;
       bool ok = true;
-      const uint32_t s0 = smem_addr(smem);
-      const uint64_t ad0 = smem_desc_sw128(s0, 16, 1024);
-      const uint64_t bd0 = smem_desc_sw128(s0 + kATileBytes, kBoxBytes, 1024);
+      const uint32_t s_b = smem_addr(st_s);
+      const uint64_t ad0 = smem_desc_sw128(s_b, 16, 1024);
+      const uint64_t bd0 = smem_desc_sw128(s_b + kATileBytes, kBoxBytes, 1024);
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
         for (int g = 0; g < G && ok; ++g, ++unit) {
-          const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4), N = 64 * nc;
+          const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4);
           ok = mbar_wait(&pb->acce[buf], (use & 1) ^ 1, &g_pf_wait_timeouts);
           if (!ok) break;
           tc_fence_after();
           const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NG);
-          const uint32_t idn = idesc_f16(BF16, kBM, N, false, true);
+          const uint32_t idn = idesc_f16(BF16, kBM, 64 * nc, false, true);
           for (int kb = 0; kb < nk; ++kb, ++it) {
             const int st = it % kUpStages;
             ok = mbar_wait(&pb->full[st], (it / kUpStages) & 1, &g_pf_wait_timeouts);
@@ -533,8 +595,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
             const uint64_t so = static_cast<uint64_t>((st * stage_bytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kBK / 16; ++kk)
-              mma_f16(dbase, ad0 + so + static_cast<uint64_t>(kk * 2), bd0 + so + static_cast<uint64_t>(kk * 128), idn,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
+              mma_f16(dbase, ad0 + so + static_cast<uint64_t>(kk * 2), bd0 + so + static_cast<uint64_t>(kk * 128),
+                      idn, (kb > 0 || kk > 0) ? 1u : 0u);
             mma_commit(&pb->empty[st]);
           }
           mma_commit(&pb->accf[buf]);
@@ -548,7 +610,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     // hide each other's latency).
     const int ew = warp - 2, lq = warp & 3, hc = ew >> 2;
     const int row = lq * 32 + lane;
-    int unit = 0;
+    int unit = 0, hseq = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
@@ -560,33 +622,35 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
       for (int g = 0; g < G; ++g, ++unit) {
         const int buf = unit & 1, use = unit >> 1, nc = min(4, C - g * 4);
         ok = mbar_wait(&pb->accf[buf], use & 1, &g_pf_wait_timeouts) && ok;
-        ok = mbar_wait(&pb->hnf[buf], use & 1, &g_pf_wait_timeouts) && ok;
         tc_fence_after();
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NG);
-        for (int cc = 0; cc < nc; ++cc) {
+        for (int cc = 0; cc < nc; ++cc, ++hseq) {
+          const int q = hseq % NH;
           uint32_t up[16];
           tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up);
+          ok = mbar_wait(&pb->hnf[q], (hseq / NH) & 1, &g_pf_wait_timeouts) && ok;
           // row `row` of this branch's hn box; 16-byte chunk j of a row sits
           // at chunk (j ^ (row & 7)) under the 128-byte swizzle
-          const uint8_t* rb = hn_s + (buf * GC + cc) * kHnBoxBytes + row * 128;
+          const uint8_t* rb = hn_s + q * kHnBoxBytes + row * 128;
           const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
           const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pb->hne[q]);
           float hf[16];
           V8<T>::unpack(v0, hf);
           V8<T>::unpack(v1, hf + 8);
           tmem_ld_wait();
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const float gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
+            float gt;
+            if constexpr (BF16) gt = sig_table(sig, bf16_code(__uint_as_float(up[j])));
+            else gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
             acc[j] = __fadd_rn(acc[j], __fmul_rn(hf[j], gt));
           }
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&pb->acce[buf]);
-          mbar_arrive(&pb->hne[buf]);
-        }
+        if (lane == 0) mbar_arrive(&pb->acce[buf]);
       }
       if (live) {
         float o[16];
@@ -659,6 +723,22 @@ bool make_chunk_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner,
   const cuuint64_t dims[3] = {64, outer, inner / 64};
   const cuuint64_t strides[2] = {inner * 2, 128};
   const cuuint32_t box[3] = {64, box_rows, static_cast<cuuint32_t>(inner / 64)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
+            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D map viewing a row-major [R, C*H] 16-bit matrix as [C branches][R rows]
+// [H columns]; box {64 columns, 64 rows, gc branches}, 128-byte swizzle: one
+// copy lands a K block of 64 columns of gc consecutive branches, branch after
+// branch, each a 128-byte-swizzled MN-major block.
+bool make_branch_map(CUtensorMap* m, const void* base, bool bf16, uint64_t H, uint64_t R, uint64_t C, uint32_t gc) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {H, R, C};
+  const cuuint64_t strides[2] = {C * H * 2, H * 2};
+  const cuuint32_t box[3] = {64, 64, gc};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base),
             dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -762,7 +842,8 @@ cudaError_t run_prefill(const Problem& p) {
   if (e != cudaSuccess) return e;
 
   PfUpArgs<T> ua;
-  if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_map(&ua.tm_b, p.up_w, BF16, CH, R, 64) ||
+  const int GC = C < 4 ? C : 4;
+  if (!make_map(&ua.tm_a, d, BF16, R, rows, kBM) || !make_branch_map(&ua.tm_b, p.up_w, BF16, H, R, C, GC) ||
       !make_tile_map(&ua.tm_hn, hn, BF16, hn_tiles))
     return cudaErrorInvalidValue;
   ua.hn = hn;
@@ -771,10 +852,14 @@ cudaError_t run_prefill(const Problem& p) {
   ua.C = C; ua.H = H; ua.R = R;
   ua.rho = p.rho;
   ua.stages = kUpStages;
-  ua.nbuf = 2;
-  const int GC = C < 4 ? C : 4;
-  const size_t usm = 1024 + static_cast<size_t>(kUpStages) * (kATileBytes + GC * kBoxBytes) +
-                     2 * static_cast<size_t>(GC) * kHnBoxBytes + sizeof(UpBars);
+  // shared memory: the operand stages, the sigmoid table and barriers, then
+  // as many hn slots (2..6) as the budget leaves
+  const size_t fixed = 1024 + static_cast<size_t>(kUpStages) * (kATileBytes + GC * kBoxBytes) + kSigBytes +
+                       sizeof(UpBars);
+  const int nh = static_cast<int>(std::min<size_t>(kHnSlotsMax, (kSmemBudget - fixed) / kHnBoxBytes));
+  if (nh < 2) return cudaErrorInvalidValue;
+  ua.nbuf = nh;
+  const size_t usm = fixed + static_cast<size_t>(nh) * kHnBoxBytes;
   e = ensure_smem<pf_up<T, BF16>>(usm);
   if (e != cudaSuccess) return e;
   const int n_tiles = static_cast<int>(mtiles) * (H / 64);
