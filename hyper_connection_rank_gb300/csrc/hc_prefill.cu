@@ -91,12 +91,14 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
     const int v = tid + i * nthr;
     if (v < NV) {
       const int c = v / NVH;
+      // each rounding to T happens once, in the pack that stores the value
+      // (S = rT(streams + gate * prev): multiply, add, then the pack rounds)
       if (pro) {
         float s8[8], p8[8];
         V8<T>::unpack(sv[i], s8);
         V8<T>::unpack(pv[i], p8);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) s8[j] = prologue_s<T>(s8[j], gt[i], p8[j]);
+        for (int j = 0; j < 8; ++j) s8[j] = __fadd_rn(s8[j], __fmul_rn(gt[i], p8[j]));
         sv[i] = V8<T>::pack(s8);
       }
       if (sout != nullptr) st16(sout + b * CH + v * 8, sv[i]);
@@ -130,8 +132,9 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
       float s8[8], n8[8], h8[8];
       V8<T>::unpack(sv[i], s8);
       V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);
+      // hn = rT((S * inv) * ns): its one rounding is the pack that stores it
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h8[j] = norm_hn<T>(s8[j], iv, n8[j]);
+      for (int j = 0; j < 8; ++j) h8[j] = __fmul_rn(__fmul_rn(s8[j], iv), n8[j]);
       // tile (b / 128, v / 8), row b % 128, 16-byte chunk v % 8
       const int64_t tile = (b >> 7) * (CH >> 6) + (v >> 3);
       st16(hn + ((tile << 7) + (b & 127)) * 64 + (v & 7) * 8, V8<T>::pack(h8));
