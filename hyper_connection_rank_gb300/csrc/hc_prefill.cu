@@ -53,36 +53,46 @@ constexpr int kNormMaxThreads = 512; // so C*H <= 512 * 4 * 8 = 16384
 
 // ---------------------------------------------------------------- pf_norm --
 
-// At most 64 registers (3 CTAs of 320 threads per SM): the loads in flight are
-// what keeps this streaming kernel near the copy bandwidth.
+// One CTA per row. The row (streams, and prev_out with a prologue) comes into
+// shared memory by one bulk copy per tensor, so no register holds load data
+// and several CTAs per SM have their rows in flight at once; S goes back to
+// shared memory in place of streams for the second pass.
 template <typename T, int C>
-__global__ void __launch_bounds__(kNormMaxThreads, 2)
+__global__ void __launch_bounds__(kNormMaxThreads)
 pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* __restrict__ prev_gate,
         const T* __restrict__ ns, int H, float eps, T* __restrict__ sout, T* __restrict__ hn) {
-  pdl_wait();
-  pdl_trigger();
+  extern __shared__ __align__(16) uint8_t row_s[];  // [C*H] streams -> S, then [H] prev_out
+  __shared__ uint64_t bar;
   __shared__ float red[C][kNormMaxThreads / 32];
   __shared__ float inv_s[C];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nthr = blockDim.x, nwarps = nthr >> 5;
   const int64_t b = blockIdx.x;
   const int CH = C * H, NV = CH / 8, NVH = H / 8;
   const bool pro = prev_out != nullptr;
-  // every load of this thread first (one round trip), then the arithmetic;
-  // norm_scale (the same for every row, cache-resident) is read at the end
-  uint4 sv[kNormVec], pv[kNormVec];
+  T* srow = reinterpret_cast<T*>(row_s);
+  const T* prow = srow + CH;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  if (tid == 0) {
+    const uint32_t sb = static_cast<uint32_t>(CH * sizeof(T)), pb = pro ? static_cast<uint32_t>(H * sizeof(T)) : 0u;
+    mbar_arrive_expect_tx(&bar, sb + pb);
+    bulk_g2s(row_s, streams + b * CH, sb, &bar);
+    if (pro) bulk_g2s(row_s + sb, prev_out + b * H, pb, &bar);
+  }
   float gt[kNormVec];
+  if (pro) {
 #pragma unroll
-  for (int i = 0; i < kNormVec; ++i) {
-    const int v = tid + i * nthr;
-    if (v < NV) {
-      const int c = v / NVH, h0 = (v - c * NVH) * 8;
-      sv[i] = ld16(streams + b * CH + v * 8);
-      if (pro) {
-        pv[i] = ld16(prev_out + b * H + h0);
-        gt[i] = ldf(prev_gate + b * C + c);
-      }
+    for (int i = 0; i < kNormVec; ++i) {
+      const int v = tid + i * nthr;
+      gt[i] = v < NV ? ldf(prev_gate + b * C + v / NVH) : 0.0f;
     }
   }
+  const bool ok = mbar_wait(&bar, 0, &g_pf_wait_timeouts);
   float ss[C];
 #pragma unroll
   for (int c = 0; c < C; ++c) ss[c] = 0.0f;
@@ -90,20 +100,22 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
   for (int i = 0; i < kNormVec; ++i) {
     const int v = tid + i * nthr;
     if (v < NV) {
-      const int c = v / NVH;
+      const int c = v / NVH, h0 = (v - c * NVH) * 8;
+      uint4 sv = *reinterpret_cast<const uint4*>(srow + v * 8);
       // each rounding to T happens once, in the pack that stores the value
       // (S = rT(streams + gate * prev): multiply, add, then the pack rounds)
       if (pro) {
         float s8[8], p8[8];
-        V8<T>::unpack(sv[i], s8);
-        V8<T>::unpack(pv[i], p8);
+        V8<T>::unpack(sv, s8);
+        V8<T>::unpack(*reinterpret_cast<const uint4*>(prow + h0), p8);
 #pragma unroll
         for (int j = 0; j < 8; ++j) s8[j] = __fadd_rn(s8[j], __fmul_rn(gt[i], p8[j]));
-        sv[i] = V8<T>::pack(s8);
+        sv = V8<T>::pack(s8);
+        *reinterpret_cast<uint4*>(srow + v * 8) = sv;  // this thread's own vector: no race
       }
-      if (sout != nullptr) st16(sout + b * CH + v * 8, sv[i]);
+      if (sout != nullptr) st16(sout + b * CH + v * 8, sv);
       float s8[8];
-      V8<T>::unpack(sv[i], s8);
+      V8<T>::unpack(sv, s8);
       float q = 0.0f;
 #pragma unroll
       for (int j = 0; j < 8; ++j) q = fmaf(s8[j], s8[j], q);
@@ -130,11 +142,11 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
     if (v < NV) {
       const float iv = inv_s[v / NVH];
       float s8[8], n8[8], h8[8];
-      V8<T>::unpack(sv[i], s8);
+      V8<T>::unpack(*reinterpret_cast<const uint4*>(srow + v * 8), s8);
       V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);
       // hn = rT((S * inv) * ns): its one rounding is the pack that stores it
 #pragma unroll
-      for (int j = 0; j < 8; ++j) h8[j] = __fmul_rn(__fmul_rn(s8[j], iv), n8[j]);
+      for (int j = 0; j < 8; ++j) h8[j] = ok ? __fmul_rn(__fmul_rn(s8[j], iv), n8[j]) : __int_as_float(0x7fc00000);
       // tile (b / 128, v / 8), row b % 128, 16-byte chunk v % 8
       const int64_t tile = (b >> 7) * (CH >> 6) + (v >> 3);
       st16(hn + ((tile << 7) + (b & 127)) * 64 + (v & 7) * 8, V8<T>::pack(h8));
@@ -795,19 +807,20 @@ cudaError_t run_prefill(const Problem& p) {
   const int64_t rows = p.rows;
   cudaError_t e;
 
+  const size_t nsm = static_cast<size_t>(CH + (p.prev_out != nullptr ? H : 0)) * sizeof(T);
   auto norm = [&](auto kern) {
     const int nv = CH / 8;
     const unsigned nthr = static_cast<unsigned>(std::max(32, (nv + kNormVec - 1) / kNormVec + 31) / 32 * 32);
-    return launch_pdl(kern, dim3(static_cast<unsigned>(rows)), dim3(nthr), 0, p.stream, 1u,
+    return launch_pdl(kern, dim3(static_cast<unsigned>(rows)), dim3(nthr), nsm, p.stream, 1u,
                       static_cast<const T*>(p.streams), static_cast<const T*>(p.prev_out),
                       static_cast<const T*>(p.prev_gate), static_cast<const T*>(p.norm_scale), H, p.eps,
                       static_cast<T*>(p.streams_out), hn);
   };
   switch (C) {
-    case 1: e = norm(pf_norm<T, 1>); break;
-    case 2: e = norm(pf_norm<T, 2>); break;
-    case 4: e = norm(pf_norm<T, 4>); break;
-    default: e = norm(pf_norm<T, 8>); break;
+    case 1: e = ensure_smem<pf_norm<T, 1>>(nsm); if (e == cudaSuccess) e = norm(pf_norm<T, 1>); break;
+    case 2: e = ensure_smem<pf_norm<T, 2>>(nsm); if (e == cudaSuccess) e = norm(pf_norm<T, 2>); break;
+    case 4: e = ensure_smem<pf_norm<T, 4>>(nsm); if (e == cudaSuccess) e = norm(pf_norm<T, 4>); break;
+    default: e = ensure_smem<pf_norm<T, 8>>(nsm); if (e == cudaSuccess) e = norm(pf_norm<T, 8>); break;
   }
   if (e != cudaSuccess) return e;
 
