@@ -655,12 +655,14 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           V8<T>::unpack(v0, hf);
           V8<T>::unpack(v1, hf + 8);
           tmem_ld_wait();
+          // hn * g is exact in fp32 (two 16-bit significands), so the fused
+          // multiply-add gives the bits of the separate multiply and add
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float gt;
             if constexpr (BF16) gt = sig_table(sig, bf16_code(__uint_as_float(up[j])));
             else gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
-            acc[j] = __fadd_rn(acc[j], __fmul_rn(hf[j], gt));
+            acc[j] = fmaf(hf[j], gt, acc[j]);
           }
         }
         tc_fence_before();
