@@ -84,12 +84,21 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
     bulk_g2s(row_s, streams + b * CH, sb, &bar);
     if (pro) bulk_g2s(row_s + sb, prev_out + b * H, pb, &bar);
   }
+  // branch of each of this thread's vectors, v / NVH without an integer
+  // divide: (v + 1/2) / NVH in fp32 is within 1e-6 of a value at least
+  // 1/(2 NVH) away from an integer (v < 2^11, quotient <= 8), so truncation
+  // is exact
+  const float rnvh = 1.0f / static_cast<float>(NVH);
+  int cv[kNormVec];
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i)
+    cv[i] = min(C - 1, static_cast<int>((static_cast<float>(tid + i * nthr) + 0.5f) * rnvh));
   float gt[kNormVec];
   if (pro) {
 #pragma unroll
     for (int i = 0; i < kNormVec; ++i) {
       const int v = tid + i * nthr;
-      gt[i] = v < NV ? ldf(prev_gate + b * C + v / NVH) : 0.0f;
+      gt[i] = v < NV ? ldf(prev_gate + b * C + cv[i]) : 0.0f;
     }
   }
   const bool ok = mbar_wait(&bar, 0, &g_pf_wait_timeouts);
@@ -100,7 +109,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
   for (int i = 0; i < kNormVec; ++i) {
     const int v = tid + i * nthr;
     if (v < NV) {
-      const int c = v / NVH, h0 = (v - c * NVH) * 8;
+      const int c = cv[i], h0 = (v - c * NVH) * 8;
       uint4 sv = *reinterpret_cast<const uint4*>(srow + v * 8);
       // each rounding to T happens once, in the pack that stores the value
       // (S = rT(streams + gate * prev): multiply, add, then the pack rounds)
@@ -140,7 +149,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
   for (int i = 0; i < kNormVec; ++i) {
     const int v = tid + i * nthr;
     if (v < NV) {
-      const float iv = inv_s[v / NVH];
+      const float iv = inv_s[cv[i]];
       float s8[8], n8[8], h8[8];
       V8<T>::unpack(*reinterpret_cast<const uint4*>(srow + v * 8), s8);
       V8<T>::unpack(__ldg(reinterpret_cast<const uint4*>(ns + v * 8)), n8);

@@ -264,7 +264,8 @@ def test_cross_path_agreement(hc):
 
 # ------------------------------------------------- prefill (tensor cores) --
 
-PREFILL_SHAPES = [(4, 2560, 320), (8, 1280, 320), (1, 4096, 64), (2, 128, 64), (8, 64, 128), (4, 256, 448)]
+PREFILL_SHAPES = [(4, 2560, 320), (8, 1280, 320), (1, 4096, 64), (2, 128, 64), (8, 64, 128), (4, 256, 448),
+                  (1, 16384, 64)]  # the last: a 64 KB row for the norm kernel
 
 
 @pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "C%d_H%d_R%d" % s)
