@@ -409,18 +409,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
 // down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
 // inject likewise -> post_gate.
 // One thread per 4 down columns (float4 partial loads, one 8-byte store of d)
-// or per inject column. ScaledSiLU's gate uses the fast sigmoid that matches
-// the accurate one bit for bit on T inputs.
+// or per inject column: thread x of a block row handles column group x of
+// row (blockIdx.x * kMidRows + y), R/4 + C <= kMidCols. ScaledSiLU's gate
+// uses the fast sigmoid that matches the accurate one bit for bit on T inputs.
+constexpr int kMidCols = 128, kMidRows = 2;
 template <typename T>
-__global__ void __launch_bounds__(256) pf_mid(const float* __restrict__ part, int ksplit, int64_t rows, int R,
-                                              int C, Attrs at, T* __restrict__ d, T* __restrict__ post) {
+__global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __restrict__ part, int ksplit,
+                                                              int64_t rows, int R, int C, Attrs at, T* __restrict__ d,
+                                                              T* __restrict__ post) {
   pdl_wait();
   pdl_trigger();
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int R4 = R / 4, W = R4 + C, NP = R + 16;
-  if (i >= rows * W) return;
-  const int64_t row = i / W;
-  const int j = static_cast<int>(i - row * W);
+  const int j = threadIdx.x;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * kMidRows + threadIdx.y;
+  if (row >= rows || j >= W) return;
   if (j < R4) {
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int ks = 0; ks < ksplit; ++ks) {
@@ -861,9 +863,9 @@ cudaError_t run_prefill(const Problem& p) {
   e = launch_pdl(pf_down<BF16>, dim3(gx, ksplit), dim3(kTcThreads), dsm, p.stream, static_cast<unsigned>(cs), da);
   if (e != cudaSuccess) return e;
 
-  const int64_t nmid = rows * (R / 4 + C);
   const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
-  e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((nmid + 255) / 256)), dim3(256), 0, p.stream, 1u,
+  e = launch_pdl(pf_mid<T>, dim3(static_cast<unsigned>((rows + kMidRows - 1) / kMidRows)), dim3(kMidCols, kMidRows), 0,
+                 p.stream, 1u,
                  static_cast<const float*>(part), static_cast<int>(ksplit), rows, R, C, at, d,
                  static_cast<T*>(p.post_gate));
   if (e != cudaSuccess) return e;
