@@ -402,7 +402,9 @@ def sweep(hc, I, dev, pk):
     flags = hc.HC_FLAG_WEIGHTS_STATIC
     for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
         weights = [I.make_weights(C, H, R, dt, seed=0, block=i, device=dev) for i in range(NSETS)]
-        for rows in (1, 2, 4, 8):
+        # rows 1-8 take the decode path; 16 / 64 / 256 (bf16) the prefill path's
+        # small-batch regime, measured the same way (weights rotate past L2)
+        for rows in ((1, 2, 4, 8, 16, 64, 256) if dt == "bf16" else (1, 2, 4, 8)):
             bufs = [I.make_activations(rows, C, H, dt, seed=0, block=0, prologue=True, device=dev)]
             bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
             ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, tdt, flags)), dtype=torch.uint8, device=dev)
@@ -443,7 +445,9 @@ def sweep(hc, I, dev, pk):
             us96 = 1000 * best[96] / 96
             slope = 1000 * (best[96] - best[48]) / 48
             b = block_bytes(rows, C, H, R, 2)
-            out[f"decode_rows{rows}_{dt}"] = {
+            name = f"decode_rows{rows}_{dt}" if rows <= 8 else f"rows{rows}_{dt}"
+            out[name] = {
+                "path": hc.PATH_NAMES[hc.path(rows, C, H, R, tdt, flags)],
                 "us_per_block": round(us96, 3), "us_per_block_slope": round(slope, 3),
                 "rows_per_s": round(rows / (us96 * 1e-6), 1),
                 "hbm_frac": round(b / (us96 * 1e-6) / 1e9 / pk["hbm"], 4),
