@@ -478,7 +478,7 @@ constexpr uint32_t kSigPosHi = 0x4100u;     // 8.0
 constexpr uint32_t kSigNegHi = 0x42C0u;     // 96.0
 constexpr int kSigPosN = static_cast<int>(kSigPosHi - kSigLo + 1);
 constexpr int kSigN = kSigPosN + static_cast<int>(kSigNegHi - kSigLo + 1);
-constexpr int kSigBytes = (kSigN * 2 + 127) / 128 * 128;
+constexpr int kSigBytes = (kSigN * 4 + 127) / 128 * 128;  // fp32 entries
 
 struct UpBars {
   uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[kHnSlotsMax], hne[kHnSlotsMax];
@@ -492,18 +492,16 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   return c;
 }
 
-__device__ __forceinline__ uint32_t bf16_code(float x) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(x)));
-}
-
-// g for the bf16 code c of u, from the table (see above).
-__device__ __forceinline__ float sig_table(const uint16_t* tab, uint32_t c) {
-  const uint32_t mag = c & 0x7FFFu, neg = c >> 15;
-  const uint32_t hi = neg ? kSigNegHi : kSigPosHi;
-  const uint32_t m2 = min(max(mag, kSigLo), hi);
-  const uint32_t idx = m2 - kSigLo + (neg ? static_cast<uint32_t>(kSigPosN) : 0u);
-  const uint32_t g = mag > 0x7F80u ? 0x7FC0u : static_cast<uint32_t>(tab[idx]);
-  return __uint_as_float(g << 16);
+// g for a bf16 value u (already rounded), from the table (see above). The
+// clamps run on the fp32 pipe and keep u a bf16 value (the bounds are bf16
+// values), so its table position is its fp32 bit pattern's top half: only two
+// shifts and a multiply-add of integer work per element.
+__device__ __forceinline__ float sig_table(const float* tab, float u) {
+  const float v = fminf(fmaxf(u, -96.0f), 8.0f);
+  const float a = fmaxf(fabsf(v), __uint_as_float(kSigLo << 16));
+  const uint32_t code = __float_as_uint(a) >> 16, neg = __float_as_uint(v) >> 31;
+  const float g = tab[code + neg * static_cast<uint32_t>(kSigPosN) - kSigLo];
+  return u == u ? g : u;  // NaN stays NaN
 }
 
 template <typename T, bool BF16>
@@ -517,7 +515,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
   const int stage_bytes = kATileBytes + GC * kBoxBytes;  // d box, then W_u of one K block for the group
   uint8_t* st_s = smem;                                  // [kUpStages][d box | GC][...]
   uint8_t* hn_s = st_s + kUpStages * stage_bytes;        // [NH][128 rows][64] (swizzled)
-  uint16_t* sig = reinterpret_cast<uint16_t*>(hn_s + NH * kHnBoxBytes);
+  float* sig = reinterpret_cast<float*>(hn_s + NH * kHnBoxBytes);
   UpBars* pb = reinterpret_cast<UpBars*>(reinterpret_cast<uint8_t*>(sig) + kSigBytes);
   const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
   const uint32_t ncols = tmem_cols_for(2 * NG);
@@ -526,7 +524,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     // the table: code of rT(sigmoid_acc(u)) for every u it covers
     for (int i = threadIdx.x; i < kSigN; i += blockDim.x) {
       const uint32_t c = i < kSigPosN ? kSigLo + i : 0x8000u | (kSigLo + (i - kSigPosN));
-      sig[i] = static_cast<uint16_t>(bf16_code(sigmoid_acc(__uint_as_float(c << 16))));
+      sig[i] = rT<__nv_bfloat16>(sigmoid_acc(__uint_as_float(c << 16)));
     }
   }
   if (warp == 0 && lane == 0) {
@@ -660,8 +658,6 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           const uint8_t* rb = hn_s + q * kHnBoxBytes + row * 128;
           const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
           const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&pb->hne[q]);
           float hf[16];
           V8<T>::unpack(v0, hf);
           V8<T>::unpack(v1, hf + 8);
@@ -671,10 +667,15 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             float gt;
-            if constexpr (BF16) gt = sig_table(sig, bf16_code(__uint_as_float(up[j])));
+            if constexpr (BF16) gt = sig_table(sig, rT<T>(__uint_as_float(up[j])));
             else gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
             acc[j] = fmaf(hf[j], gt, acc[j]);
           }
+          // the slot is released only after every lane has used what it read
+          // from it (a release right after issuing the loads let the next box
+          // land under loads still in flight)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&pb->hne[q]);
         }
         tc_fence_before();
         __syncwarp();
