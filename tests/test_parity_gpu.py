@@ -298,6 +298,22 @@ def test_prefill_large_batch_regime(hc):
             assert np.array_equal(a[lo:hi], b)
 
 
+@pytest.mark.parametrize("dt,C,H", [("bf16", 4, 2560), ("f16", 8, 1280)])
+def test_prefill_full_size_row_invariance(hc, dt, C, H):
+    """At the 8192-row prefill shapes every output of a row is bitwise the
+    same in the full call and in calls on two sub-batches (other tile
+    positions, other CTAs, a ragged last tile): catches any exchange between
+    rows, including a producer that overwrites a buffer a consumer still reads."""
+    R = 320
+    d = I.make_block(8192, C, H, R, dt, seed=31, prologue=True)
+    full = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    for lo, hi in ((0, 4096), (1000, 8192)):
+        sub = {k: (v[lo:hi] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+        part = run_gpu(hc, sub, C, I.QWEN_ATTRS)
+        for a, b in zip(full, part):
+            assert np.array_equal(a[lo:hi], b)
+
+
 def test_prefill_row_independence_bitwise(hc):
     """Within the prefill path a row's bits do not depend on the batch: rows
     of a 300-row call equal the same rows in 137- and 150-row calls (different
