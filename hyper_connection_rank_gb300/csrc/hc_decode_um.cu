@@ -310,7 +310,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     const int q = p & 3, mt = p >> 2;
     uint32_t v[16];
     tmem_ld16_nowait(tmem + (static_cast<uint32_t>(q * 32) << 16) + mt * kUmRowsN, v);
-    tmem_ld_wait();
+    tmem_ld_wait_r(v);
     const int col = p * 32 + lane;  // = mt * 128 + q * 32 + lane
     if (col < NCP) {
       const int ow = col / OC, lc = col - ow * OC;
@@ -587,7 +587,9 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
 #pragma unroll
     for (int j = 0; j < kUpIssuers; ++j)
       if (j < NI) tmem_ld16_nowait(tq + j * kUmRowsN, acc[j]);
-    tmem_ld_wait();
+#pragma unroll
+    for (int j = 0; j < kUpIssuers; ++j)
+      if (j < NI) tmem_ld_wait_r(acc[j]);
     float v[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {

@@ -650,8 +650,6 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
         const uint32_t taddr = tmem + (static_cast<uint32_t>(lq * 32) << 16) + static_cast<uint32_t>(buf * NG);
         for (int cc = 0; cc < nc; ++cc, ++hseq) {
           const int q = hseq % NH;
-          uint32_t up[16];
-          tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up);
           ok = mbar_wait(&pb->hnf[q], (hseq / NH) & 1, &g_pf_wait_timeouts) && ok;
           // row `row` of this branch's hn box; 16-byte chunk j of a row sits
           // at chunk (j ^ (row & 7)) under the 128-byte swizzle
@@ -661,7 +659,12 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           float hf[16];
           V8<T>::unpack(v0, hf);
           V8<T>::unpack(v1, hf + 8);
-          tmem_ld_wait();
+          // the wait names the loaded registers (tmem_ld_wait_r), so no use of
+          // them is scheduled above it (a bare wait let the fp16 sigmoid read
+          // registers the load had not filled: nondeterministic results)
+          uint32_t up[16];
+          tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up);
+          tmem_ld_wait_r(up);
           // hn * g is exact in fp32 (two 16-bit significands), so the fused
           // multiply-add gives the bits of the separate multiply and add
 #pragma unroll
@@ -672,8 +675,11 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
             acc[j] = fmaf(hf[j], gt, acc[j]);
           }
           // the slot is released only after every lane has used what it read
-          // from it (a release right after issuing the loads let the next box
-          // land under loads still in flight)
+          // from it, and each lane first orders its (generic-proxy) reads
+          // before the refill, a TMA write of the async proxy: without the
+          // proxy fence the refill could overtake the reads (seen as rows of a
+          // 16-feature chunk taking the next box's values)
+          fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&pb->hne[q]);
         }
