@@ -298,6 +298,18 @@ def test_prefill_large_batch_regime(hc):
             assert np.array_equal(a[lo:hi], b)
 
 
+@pytest.mark.parametrize("dt,C,H", [("bf16", 4, 2560), ("f16", 4, 2560), ("bf16", 8, 1280), ("f16", 8, 1280)])
+def test_prefill_full_size_deterministic(hc, dt, C, H):
+    """Repeated 8192-row calls give identical bits in both 16-bit types (a
+    race between a consumer's reads and a producer's refill shows here first)."""
+    d = I.make_block(8192, C, H, 320, dt, seed=37, prologue=True)
+    first = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    for _ in range(4):
+        again = run_gpu(hc, d, C, I.QWEN_ATTRS)
+        for a, b in zip(first, again):
+            assert np.array_equal(a, b)
+
+
 @pytest.mark.parametrize("dt,C,H", [("bf16", 4, 2560), ("f16", 8, 1280)])
 def test_prefill_full_size_row_invariance(hc, dt, C, H):
     """At the 8192-row prefill shapes every output of a row is bitwise the
