@@ -296,6 +296,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       uint8_t* sp = smem + st * stage_bytes;
       uint8_t* bsp = sp + kATileBytes;
       const int k = k_begin + it * kBK;
+      // the stage's previous MMAs (async proxy) read this inject chunk; order
+      // those reads before the generic writes below
+      fence_proxy_async_smem();
       for (int kr = lane; kr < kBK; kr += 32) {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(wi_s) + static_cast<int64_t>(k - k_begin + kr) * C;
         const int p = kr / prow, r = kr - p * prow;

@@ -198,13 +198,15 @@ engram_gate_kernel(const T* __restrict__ key, const T* __restrict__ query, const
           Vec16<T>::unpack(zq[j], sq);
           pk[j] = sumsq<VE>(fk);
           pq[j] = sumsq<VE>(fq);
-          float c[VE];
+          // cross term: (key * ks) * (query * qs), the last product fused into
+          // the pairwise sum (two accumulators, added at the end)
+          float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-          for (int e = 0; e < VE; ++e) c[e] = __fmul_rn(__fmul_rn(fk[e], sk[e]), __fmul_rn(fq[e], sq[e]));
-          float sacc = __fadd_rn(c[0], c[1]);
-#pragma unroll
-          for (int e = 2; e < VE; e += 2) sacc = __fadd_rn(sacc, __fadd_rn(c[e], c[e + 1]));
-          pc[j] = sacc;
+          for (int e = 0; e < VE; e += 2) {
+            s0 = fmaf(__fmul_rn(fk[e], sk[e]), __fmul_rn(fq[e], sq[e]), s0);
+            s1 = fmaf(__fmul_rn(fk[e + 1], sk[e + 1]), __fmul_rn(fq[e + 1], sq[e + 1]), s1);
+          }
+          pc[j] = __fadd_rn(s0, s1);
         }
         acc[0] = __fadd_rn(acc[0], __fadd_rn(pk[0], pk[1]));
         acc[1] = __fadd_rn(acc[1], __fadd_rn(pq[0], pq[1]));
