@@ -305,8 +305,8 @@ def profile_rowops(args, hc, I, dev):
 
 
 def e2e_measure(args, hc, I, weights, dev, flags):
-    """Same metric through the public API with host buffers: every step copies
-    its inputs host->device from pinned memory, runs the block, and reads its
+    """Same metric through the C ABI with host buffers: every step copies its
+    inputs host->device from pinned memory, calls hc_lowrank_mix, and reads its
     outputs back device->host."""
     import torch
     rows = 1
@@ -334,12 +334,25 @@ def e2e_measure(args, hc, I, weights, dev, flags):
     dev_out_buf, dev_out = packed(out_shapes, dev, False)
     ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
     n = max(1, min(args.steps, args.e2e_steps))
+    # the C-ABI call itself (hc_lowrank_mix through ctypes), its attribute
+    # struct and device addresses prepared once: what a host program calling
+    # the library pays per block, plus the two copies
+    from hyper_connection_rank_gb300 import _binding as B
+    attrs = B.make_attrs(flags=flags, **QWEN)
+    stream = torch.cuda.current_stream(dev).cuda_stream
+    act = [t.data_ptr() for t in dev_in]
+    outs = [t.data_ptr() for t in dev_out]
+    wps = [[w[k].data_ptr() for k in ("norm_scale", "down_w", "up_w", "inject_w")] for w in weights]
+    call = B.raw_call
+    wsp, wsn = ws.data_ptr(), ws.numel()
 
     def one(i):
         dev_in_buf.copy_(host_in_buf, non_blocking=True)
-        w = weights[i % NSETS]
-        hc.lowrank_mix(dev_in[0], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], dev_in[1], dev_in[2],
-                       num_branches=C, flags=flags, out=tuple(dev_out), workspace=ws, **QWEN)
+        ns, dw, uw, iw = wps[i % NSETS]
+        st = call(act[0], ns, dw, uw, iw, act[1], act[2], rows, C, H, R, attrs, B.HC_BF16, outs[0], outs[1], outs[2],
+                  wsp, wsn, stream)
+        if st != 0:
+            B.check(st)
         host_out_buf.copy_(dev_out_buf, non_blocking=True)
 
     for i in range(max(3, args.warmup)):
@@ -359,7 +372,7 @@ def e2e_measure(args, hc, I, weights, dev, flags):
     bo = host_out_buf.numel() * host_out_buf.element_size()
     return {"value": round(rows * n / t, 1), "unit": "rows/s", "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
             "steps": n, "us_per_step": round(1e6 * t / n, 3), "wall_us_per_step": round(1e6 * wall / n, 3),
-            "api": "hyper_connection_rank_gb300.lowrank_mix -> hc_lowrank_mix (C ABI), eager launches"}
+            "api": "hc_lowrank_mix (C ABI, through ctypes) with host buffers: one pinned H2D copy, the block, one D2H copy per step; eager launches"}
 
 
 def cpu_baseline(seconds):
