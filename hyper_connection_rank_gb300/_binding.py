@@ -28,7 +28,7 @@ DTYPE_CODES = {torch.float32: HC_F32, torch.float16: HC_F16, torch.bfloat16: HC_
 # Every symbol include/hc_lowrank_mix.h declares.
 EXPORTS = ("hc_attrs_default", "hc_lowrank_mix_path", "hc_lowrank_mix_workspace_size", "hc_lowrank_mix",
            "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts", "hc_debug_sigmoid_exact",
-           "hc_inv_rms", "hc_engram_gate")
+           "hc_debug_sigmoid_table", "hc_inv_rms", "hc_engram_gate")
 
 
 class HcAttrs(ctypes.Structure):
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH):
         L.hc_debug_wait_timeouts.restype = ctypes.c_uint
         L.hc_debug_sigmoid_exact.argtypes = [ci, vp, vp, vp]
         L.hc_debug_sigmoid_exact.restype = ci
+        L.hc_debug_sigmoid_table.argtypes = [vp, vp]
+        L.hc_debug_sigmoid_table.restype = ci
         f32 = ctypes.c_float
         L.hc_inv_rms.argtypes = [vp, i64, i64, f32, ci, vp, vp]
         L.hc_inv_rms.restype = ci
@@ -183,6 +185,15 @@ def debug_sigmoid_exact(dt: torch.dtype, device="cuda"):
     s = torch.cuda.current_stream(fast.device)
     check(lib().hc_debug_sigmoid_exact(DTYPE_CODES[dt], _ptr(fast), _ptr(acc), s.cuda_stream))
     return fast, acc
+
+
+def debug_sigmoid_table(device="cuda"):
+    """g for all 65536 bf16 codes of up as the bf16 prefill epilogue forms it,
+    as a float32 tensor on `device` (see hc_debug_sigmoid_table)."""
+    g = torch.empty(65536, dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream(g.device)
+    check(lib().hc_debug_sigmoid_table(_ptr(g), s.cuda_stream))
+    return g
 
 
 def _check_cuda(name, t, dt):

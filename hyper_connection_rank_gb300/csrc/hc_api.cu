@@ -240,6 +240,13 @@ hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_o
   return HC_OK;
 }
 
+hc_status_t hc_debug_sigmoid_table(float* g_out, struct CUstream_st* stream) {
+  if (g_out == nullptr) return hc::set_error(HC_ERR_INVALID_ARG, "null output pointer");
+  const cudaError_t e = hc::launch_sigmoid_table_codes(g_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return hc::set_error(HC_ERR_CUDA, cudaGetErrorString(e));
+  return HC_OK;
+}
+
 
 // ---------------------------------------------------------------------------
 // Row inverse RMS (FreeToken PR #101) and com.microsoft.EngramGate: declared

@@ -376,6 +376,22 @@ struct UpArgs {
   Attrs at;
 };
 
+// post_gate for every row: the inject partials summed in cluster order. One
+// CTA runs it; kept out of line so that the others never fetch its code.
+template <typename T>
+__device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool split, int B, int C, int NCLU, int NCP,
+                                           int R, bool ok, const UpArgs<T>& a) {
+  const float qnan = __int_as_float(0x7fc00000);
+  #pragma unroll 1
+  for (int i = threadIdx.x; i < B * C; i += blockDim.x) {
+    const int b = i / C, cc = i - b * C;
+    const float* src = split ? st + inj_off + static_cast<size_t>(b) * 8 + cc : st + static_cast<size_t>(b) * NCP + R + cc;
+    const size_t stride = split ? static_cast<size_t>(B) * 8 : static_cast<size_t>(B) * NCP;
+    const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
+    stf(a.post + b * C + cc, ok ? post_gate_of<T>(rT<T>(x), a.at.gate_div, a.at.gate_mul) : qnan);
+  }
+}
+
 template <typename T, int MB>
 __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
@@ -405,13 +421,15 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   const int64_t col0 = static_cast<int64_t>(c) * H + h0;
   const bool pro = a.prev_out != nullptr;
   const bool do_post = (q == 0 && c == 0);
+  // one row needs no split (the host never sets it then): the code is left out
+  const bool split = MB > 1 && a.split != 0;
 
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(dbar, 1);
     mbar_init(mbar, 1);
     mbar_init(mma_bar, min(kUpIssuers, (R + 15) / 16));  // one commit per issuing warp
-    mbar_arrive_expect_tx(dbar, a.split ? static_cast<uint32_t>(R * B * 2) : 0u);
+    mbar_arrive_expect_tx(dbar, split ? static_cast<uint32_t>(R * B * 2) : 0u);
     mbar_arrive_expect_tx(mbar, C > 1 ? static_cast<uint32_t>(C * HSc * B * 4) : 0u);
     fence_mbar_init();
   }
@@ -483,15 +501,15 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   const uint32_t tmem = *tmem_slot;
 
   // ---- pull the down partials into shared memory ----
-  const int ncols = a.split ? max(0, min(R, (c + 1) * a.per) - c * a.per) : 0;
+  const int ncols = split ? max(0, min(R, (c + 1) * a.per) - c * a.per) : 0;
   const size_t inj_off = static_cast<size_t>(NCLU) * B * a.per;  // floats (split layout)
   if (warp == 0) {
     uint32_t bytes;
-    if (!a.split) bytes = static_cast<uint32_t>(NCLU * B * NCP * 4);
+    if (!split) bytes = static_cast<uint32_t>(NCLU * B * NCP * 4);
     else bytes = static_cast<uint32_t>(NCLU * B * ncols * 4 + (do_post ? NCLU * B * 32 : 0));
     if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     __syncwarp();
-    if (!a.split) {
+    if (!split) {
       if (lane == 0) bulk_g2s(st, a.part_ws, bytes, bar);
     } else {
       #pragma unroll 1
@@ -510,7 +528,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   const float qnan = __int_as_float(0x7fc00000);
 
   // ---- d = ScaledSiLU(rT(sum of the partials in cluster order)) as T, into B ----
-  if (!a.split) {
+  if (!split) {
     const size_t stride = static_cast<size_t>(B) * NCP;
     #pragma unroll 1
     for (int i = tid; i < B * R; i += nthr) {
@@ -519,7 +537,8 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
       *reinterpret_cast<T*>(sB + b_off(b, col)) = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x), a.at.alpha) : qnan);
     }
-  } else {
+  }
+  if constexpr (MB > 1) if (split) {
     const int npair = ncols / 2;
     const size_t stride = static_cast<size_t>(B) * a.per;
     #pragma unroll 1
@@ -536,16 +555,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       for (int pr = 0; pr < C; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
     }
   }
-  if (do_post) {
-    #pragma unroll 1
-    for (int i = tid; i < B * C; i += nthr) {
-      const int b = i / C, cc = i - b * C;
-      const float* src = a.split ? st + inj_off + static_cast<size_t>(b) * 8 + cc : st + static_cast<size_t>(b) * NCP + R + cc;
-      const size_t stride = a.split ? static_cast<size_t>(B) * 8 : static_cast<size_t>(B) * NCP;
-      const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
-      stf(a.post + b * C + cc, ok ? post_gate_of<T>(rT<T>(x), a.at.gate_div, a.at.gate_mul) : qnan);
-    }
-  }
+  if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a);
   #pragma unroll 1
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
@@ -557,7 +567,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   }
   cp_async_wait_all();
   bool dok = true;
-  if (a.split) dok = mbar_wait(dbar, 0, &g_um_wait_timeouts);
+  if (split) dok = mbar_wait(dbar, 0, &g_um_wait_timeouts);
   fence_proxy_async_smem();  // A (cp.async) and B (d) visible to the tensor core
   __syncthreads();
 

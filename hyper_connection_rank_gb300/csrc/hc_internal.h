@@ -52,6 +52,7 @@ cudaError_t launch_decode_um(const Problem& p);
 unsigned int read_um_wait_timeouts(bool reset);
 // Every 16-bit code through the fast rounded sigmoid and the accurate one.
 cudaError_t launch_sigmoid_codes(hc_dtype_t dt, uint16_t* fast, uint16_t* acc, cudaStream_t s);
+cudaError_t launch_sigmoid_table_codes(float* g, cudaStream_t s);
 // Row inverse RMS and Engram gate (hc_rows.cu). `vec`: every pointer 16-byte
 // aligned and the row length a multiple of 16 bytes (16-byte vector loads).
 cudaError_t launch_inv_rms(const void* x, int64_t rows, int64_t dim, float eps, hc_dtype_t dt, float* out, bool vec,

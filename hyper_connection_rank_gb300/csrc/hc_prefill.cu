@@ -464,10 +464,16 @@ __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __res
 // the MMAs and owns the tensor memory, 2..17 run the epilogue, 18 loads hn.
 //
 // g = rT(sigmoid(u)) for u = rT(up): in bf16 it is read from a table of the
-// accurate sigmoid over every bf16 u whose result is not a constant
-// (|u| in [2^-9, 8) for u >= 0, [2^-9, 96] for u < 0; below, g = 1/2; above,
-// g = 1 resp. 0; NaN stays NaN), built by the CTA at start: bit for bit the
-// accurate rounded sigmoid, with neither MUFU operation of the formula. fp16
+// accurate sigmoid over every bf16 u whose result is not a constant, built by
+// the CTA at start: bit for bit the accurate rounded sigmoid, with neither
+// MUFU operation of the formula. Two values are looked up together: the pair
+// is rounded by one packed conversion and clamped by packed bf16 minimum and
+// maximum (to [-96, 8]: beyond, g is 0 resp. 1), then its magnitude codes
+// by packed 16-bit integer minimum and maximum (below 2^-9, g = 1/2; NaN,
+// which the clamps turn into the canonical NaN, lands on an entry holding
+// NaN); a sign bit moved to bit 11 selects the negative half of the table. The
+// table holds bf16 values and hn * g + acc is one mixed-precision fused
+// multiply-add (bf16 operands, fp32 addend): no operand is widened first. fp16
 // keeps the branch-free fast sigmoid (its rounding can differ in one ulp near
 // a rounding midpoint).
 constexpr int kUpEpiWarps = 16;
@@ -477,11 +483,12 @@ constexpr int kHnBoxBytes = 128 * 64 * 2;   // one branch: 128 rows x 64 feature
 constexpr int kUpStages = 2;
 constexpr int kHnSlotsMax = 6;
 constexpr uint32_t kSigLo = 0x3AFFu;        // largest bf16 magnitude code below 2^-9
-constexpr uint32_t kSigPosHi = 0x4100u;     // 8.0
-constexpr uint32_t kSigNegHi = 0x42C0u;     // 96.0
-constexpr int kSigPosN = static_cast<int>(kSigPosHi - kSigLo + 1);
-constexpr int kSigN = kSigPosN + static_cast<int>(kSigNegHi - kSigLo + 1);
-constexpr int kSigBytes = (kSigN * 4 + 127) / 128 * 128;  // fp32 entries
+constexpr uint32_t kSigPosHi = 0x4100u;     // 8.0: positive u are clamped here
+constexpr uint32_t kSigNegHi = 0x42C0u;     // 96.0: negative u are clamped at -96
+constexpr uint32_t kSigNaN = kSigNegHi + 1; // the magnitude code NaN is moved to
+constexpr int kSigHalf = 2048;              // entries per sign; a power of two >= kSigNaN - kSigLo + 1
+constexpr int kSigBytes = 2 * kSigHalf * 2; // bf16 entries
+static_assert(static_cast<int>(kSigNaN - kSigLo) < kSigHalf, "sigmoid table half too small");
 
 struct UpBars {
   uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[kHnSlotsMax], hne[kHnSlotsMax];
@@ -495,16 +502,51 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
   return c;
 }
 
-// g for a bf16 value u (already rounded), from the table (see above). The
-// clamps run on the fp32 pipe and keep u a bf16 value (the bounds are bf16
-// values), so its table position is its fp32 bit pattern's top half: only two
-// shifts and a multiply-add of integer work per element.
-__device__ __forceinline__ float sig_table(const float* tab, float u) {
-  const float v = fminf(fmaxf(u, -96.0f), 8.0f);
-  const float a = fmaxf(fabsf(v), __uint_as_float(kSigLo << 16));
-  const uint32_t code = __float_as_uint(a) >> 16, neg = __float_as_uint(v) >> 31;
-  const float g = tab[code + neg * static_cast<uint32_t>(kSigPosN) - kSigLo];
-  return u == u ? g : u;  // NaN stays NaN
+// Entry i of the table: sign i / kSigHalf, magnitude code kSigLo + i % kSigHalf.
+__device__ __forceinline__ uint16_t sig_entry(int i) {
+  const uint32_t neg = static_cast<uint32_t>(i) / kSigHalf, m = kSigLo + static_cast<uint32_t>(i) % kSigHalf;
+  if (m == kSigNaN) return 0x7FC0u;                      // NaN
+  if (m > (neg ? kSigNegHi : kSigPosHi)) return 0;       // never read
+  const float u = __uint_as_float(((neg << 15) | m) << 16);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(sigmoid_acc(u)));
+}
+
+// acc0 += hn0 * g(up0), acc1 += hn1 * g(up1) for a pair of bf16 hn values
+// (element 0 in the low half of hn2) and their fp32 up values, with g from
+// the table at shared-memory address tab (see above).
+__device__ __forceinline__ void sig_pair_fma(const uint16_t* tab, uint32_t hn2, float up0, float up1, float& acc0,
+                                             float& acc1) {
+  uint32_t v2, m2;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(v2) : "f"(up1), "f"(up0));
+  asm("max.NaN.bf16x2 %0, %0, %1;" : "+r"(v2) : "r"(0xC2C0C2C0u));  // -96
+  asm("min.NaN.bf16x2 %0, %0, %1;" : "+r"(v2) : "r"(0x41004100u));  // 8
+  m2 = v2 & 0x7FFF7FFFu;
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(kSigLo * 0x10001u));
+  asm("min.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(kSigNaN * 0x10001u));
+  const uint32_t idx2 = m2 + ((v2 >> 4) & 0x08000800u) - kSigLo * 0x10001u;
+  const uint16_t g0 = tab[idx2 & 0xFFFFu], g1 = tab[idx2 >> 16];
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, h0, %3, %0;\n\t"
+      "fma.rn.f32.bf16 %1, h1, %4, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(hn2), "h"(g0), "h"(g1));
+}
+
+// The epilogue's gate for every bf16 code (diagnostic for
+// hc_debug_sigmoid_table): one pair of codes per thread, hn = 1, zero sums.
+__global__ void __launch_bounds__(256) sigmoid_table_codes(float* g) {
+  __shared__ uint16_t tab[2 * kSigHalf];
+  for (int i = threadIdx.x; i < 2 * kSigHalf; i += blockDim.x) tab[i] = sig_entry(i);
+  __syncthreads();
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;  // codes 2p, 2p + 1
+  if (p >= 32768) return;
+  const float u0 = __uint_as_float(static_cast<uint32_t>(2 * p) << 16);
+  const float u1 = __uint_as_float(static_cast<uint32_t>(2 * p + 1) << 16);
+  float a0 = 0.0f, a1 = 0.0f;
+  sig_pair_fma(tab, 0x3F803F80u, u0, u1, a0, a1);  // hn = (1, 1)
+  g[2 * p] = a0;
+  g[2 * p + 1] = a1;
 }
 
 template <typename T, bool BF16>
@@ -518,17 +560,13 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
   const int stage_bytes = kATileBytes + GC * kBoxBytes;  // d box, then W_u of one K block for the group
   uint8_t* st_s = smem;                                  // [kUpStages][d box | GC][...]
   uint8_t* hn_s = st_s + kUpStages * stage_bytes;        // [NH][128 rows][64] (swizzled)
-  float* sig = reinterpret_cast<float*>(hn_s + NH * kHnBoxBytes);
+  uint16_t* sig = reinterpret_cast<uint16_t*>(hn_s + NH * kHnBoxBytes);
   UpBars* pb = reinterpret_cast<UpBars*>(reinterpret_cast<uint8_t*>(sig) + kSigBytes);
   const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
   const uint32_t ncols = tmem_cols_for(2 * NG);
 
   if (BF16) {
-    // the table: code of rT(sigmoid_acc(u)) for every u it covers
-    for (int i = threadIdx.x; i < kSigN; i += blockDim.x) {
-      const uint32_t c = i < kSigPosN ? kSigLo + i : 0x8000u | (kSigLo + (i - kSigPosN));
-      sig[i] = rT<__nv_bfloat16>(sigmoid_acc(__uint_as_float(c << 16)));
-    }
+    for (int i = threadIdx.x; i < 2 * kSigHalf; i += blockDim.x) sig[i] = sig_entry(i);
   }
   if (warp == 0 && lane == 0) {
     for (int st = 0; st < kUpStages; ++st) {
@@ -659,23 +697,27 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           const uint8_t* rb = hn_s + q * kHnBoxBytes + row * 128;
           const uint4 v0 = *reinterpret_cast<const uint4*>(rb + (((2 * hc) ^ (row & 7)) << 4));
           const uint4 v1 = *reinterpret_cast<const uint4*>(rb + (((2 * hc + 1) ^ (row & 7)) << 4));
-          float hf[16];
-          V8<T>::unpack(v0, hf);
-          V8<T>::unpack(v1, hf + 8);
           // the wait names the loaded registers (tmem_ld_wait_r), so no use of
           // them is scheduled above it (a bare wait let the fp16 sigmoid read
           // registers the load had not filled: nondeterministic results)
           uint32_t up[16];
           tmem_ld16_nowait(taddr + cc * 64 + hc * 16, up);
           tmem_ld_wait_r(up);
-          // hn * g is exact in fp32 (two 16-bit significands), so the fused
-          // multiply-add gives the bits of the separate multiply and add
+          if constexpr (BF16) {
+            const uint32_t hw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float gt;
-            if constexpr (BF16) gt = sig_table(sig, rT<T>(__uint_as_float(up[j])));
-            else gt = rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j]))));
-            acc[j] = fmaf(hf[j], gt, acc[j]);
+            for (int i = 0; i < 8; ++i)
+              sig_pair_fma(sig, hw[i], __uint_as_float(up[2 * i]), __uint_as_float(up[2 * i + 1]), acc[2 * i],
+                           acc[2 * i + 1]);
+          } else {
+            float hf[16];
+            V8<T>::unpack(v0, hf);
+            V8<T>::unpack(v1, hf + 8);
+            // hn * g is exact in fp32 (two 16-bit significands), so the fused
+            // multiply-add gives the bits of the separate multiply and add
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[j] = fmaf(hf[j], rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j])))), acc[j]);
           }
           // the slot is released only after every lane has used what it read
           // from it, and each lane first orders its (generic-proxy) reads
@@ -907,6 +949,11 @@ cudaError_t run_prefill(const Problem& p) {
 }
 
 }  // namespace
+
+cudaError_t launch_sigmoid_table_codes(float* g, cudaStream_t s) {
+  sigmoid_table_codes<<<128, 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
 
 bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   if (dt != HC_BF16 && dt != HC_F16) return false;

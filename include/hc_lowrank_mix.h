@@ -168,6 +168,18 @@ unsigned int hc_debug_wait_timeouts(int reset);
  * pointer, HC_ERR_CUDA if the launch fails. */
 hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_out, struct CUstream_st* stream);
 
+/* Diagnostic, with no counterpart on the page that defines the block: the
+ * gate g = rT(sigmoid(rT(up))) exactly as the bf16 prefill epilogue forms it
+ * (a shared-memory table of the accurate rounded sigmoid, reached through
+ * packed clamps of a pair of values, and the mixed-precision multiply-add of
+ * hn * g into an fp32 sum), evaluated with hn = 1 and a zero sum for the up
+ * value of each of the 65536 bf16 codes x, so that g_out[x] (fp32) holds g
+ * itself; it must equal the accurate rounded sigmoid of x for every code
+ * (NaN for NaN). g_out: device buffer of 65536 floats, owned by the caller.
+ * Asynchronous on `stream`. HC_ERR_INVALID_ARG for a null pointer,
+ * HC_ERR_CUDA if the launch fails. */
+hc_status_t hc_debug_sigmoid_table(float* g_out, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

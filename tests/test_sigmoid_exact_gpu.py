@@ -57,3 +57,23 @@ def test_accurate_sigmoid_matches_oracle_rounding(hc, dt):
     # NaN inputs give NaN
     nan_out = oracle.to_float(a[~finite & np.isnan(xs)], code)
     assert np.isnan(nan_out).all()
+
+
+def test_prefill_table_gate_equals_accurate_on_every_code(hc):
+    """The bf16 prefill epilogue's gate (table, packed clamps, mixed-precision
+    multiply-add) on every bf16 code of up against the accurate rounded
+    sigmoid evaluated by the library, code for code; NaN gives NaN."""
+    g = hc.debug_sigmoid_table()
+    _, acc = hc.debug_sigmoid_exact(torch.bfloat16)
+    torch.cuda.synchronize()
+    g = g.cpu().numpy()
+    a = acc.cpu().numpy().view(np.uint16)
+    xs = oracle.to_float(np.arange(65536, dtype=np.uint16), 2)
+    nan_in = np.isnan(xs)
+    assert np.isnan(g[nan_in]).all()
+    # g is a bf16 value carried in fp32: its top half is the bf16 code
+    gb = (g[~nan_in].view(np.uint32) >> 16).astype(np.uint16)
+    low = g[~nan_in].view(np.uint32) & 0xFFFF
+    assert not low.any(), "gate is not a bf16 value"
+    bad = np.nonzero(gb != a[~nan_in])[0]
+    assert bad.size == 0, f"{bad.size} codes differ, e.g. {np.arange(65536)[~nan_in][bad[:8]].tolist()}"
