@@ -480,7 +480,7 @@ constexpr int kUpEpiWarps = 16;
 constexpr int kUpHnWarp = 2 + kUpEpiWarps;                 // the warp that loads hn
 constexpr int kUpThreads = 32 * (kUpHnWarp + 1);
 constexpr int kHnBoxBytes = 128 * 64 * 2;   // one branch: 128 rows x 64 features
-constexpr int kUpStages = 2;
+constexpr int kUpStages = 3;
 constexpr int kHnSlotsMax = 6;
 constexpr uint32_t kSigLo = 0x3AFFu;        // largest bf16 magnitude code below 2^-9
 constexpr uint32_t kSigPosHi = 0x4100u;     // 8.0: positive u are clamped here
