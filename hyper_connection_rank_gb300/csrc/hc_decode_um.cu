@@ -380,7 +380,7 @@ struct UpArgs {
 // CTA runs it; kept out of line so that the others never fetch its code.
 template <typename T>
 __device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool split, int B, int C, int NCLU, int NCP,
-                                           int R, bool ok, const UpArgs<T>& a) {
+                                           int R, bool ok, T* post, float gate_div, float gate_mul) {
   const float qnan = __int_as_float(0x7fc00000);
   #pragma unroll 1
   for (int i = threadIdx.x; i < B * C; i += blockDim.x) {
@@ -388,7 +388,7 @@ __device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool
     const float* src = split ? st + inj_off + static_cast<size_t>(b) * 8 + cc : st + static_cast<size_t>(b) * NCP + R + cc;
     const size_t stride = split ? static_cast<size_t>(B) * 8 : static_cast<size_t>(B) * NCP;
     const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
-    stf(a.post + b * C + cc, ok ? post_gate_of<T>(rT<T>(x), a.at.gate_div, a.at.gate_mul) : qnan);
+    stf(post + b * C + cc, ok ? post_gate_of<T>(rT<T>(x), gate_div, gate_mul) : qnan);
   }
 }
 
@@ -555,7 +555,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       for (int pr = 0; pr < C; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
     }
   }
-  if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a);
+  if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
   #pragma unroll 1
   for (int i = tid; i < B * HS; i += nthr) {
     const int b = i / HS, h = i - b * HS;
