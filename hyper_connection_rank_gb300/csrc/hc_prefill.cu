@@ -198,15 +198,6 @@ struct PipeBars {
   uint32_t tmem_base;
 };
 
-__device__ __forceinline__ void pipe_init(PipeBars* pb, int stages) {
-  for (int s = 0; s < stages; ++s) {
-    mbar_init(&pb->full[s], 1);
-    mbar_init(&pb->empty[s], 1);
-  }
-  mbar_init(&pb->done, 1);
-  fence_mbar_init();
-}
-
 // The inject projection rides along as 16 extra N columns (chunk R/64 of
 // the B operand, C columns used, the rest zero). Its rows are too narrow for
 // a TMA copy (C * 2 bytes), so the producer warp writes them into the
@@ -857,11 +848,6 @@ bool make_branch_map(CUtensorMap* m, const void* base, bool bf16, uint64_t H, ui
 }
 
 constexpr int kSmemBudget = 220 * 1024;
-
-int pick_stages(int stage_bytes) {
-  const int s = (kSmemBudget - 1024 - static_cast<int>(sizeof(PipeBars))) / stage_bytes;
-  return std::max(1, std::min(4, s));
-}
 
 // K split of the down projection. Batches of up to kSmallRows rows have few
 // 128-row tiles, so K is cut finer (slices of 256, or the largest of 128/64
