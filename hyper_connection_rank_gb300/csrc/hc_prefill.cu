@@ -165,7 +165,7 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
 
 // ------------------------------------------------- tensor-core pipelines --
 
-struct alignas(64) PfDownArgs {
+struct PfDownArgs {
   CUtensorMap tm_a;        // hn tiles [row tiles * C*H/64][128][64], box {64 k, 128 rows, 1}
   CUtensorMap tm_b;        // down_w viewed as [R/64 column chunks][C*H rows][64 columns],
                            // box {64 columns, 64 / cs rows, R/64 chunks}
@@ -177,7 +177,7 @@ struct alignas(64) PfDownArgs {
 };
 
 template <typename T>
-struct alignas(64) PfUpArgs {
+struct PfUpArgs {
   CUtensorMap tm_a;  // d     [rows, R],   box {64 k, 128 rows}
   CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
   CUtensorMap tm_hn; // hn tiles [row tiles * C*H/64][128][64], box {64 features, 128 rows, 1}
