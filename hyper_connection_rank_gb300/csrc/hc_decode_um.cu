@@ -67,6 +67,24 @@ __host__ __device__ inline uint32_t sw128(int row, int col_in_64) {
 // B operand (activation rows x K, K-major): k-block kb of 64 holds 16 rows.
 __host__ __device__ inline uint32_t b_off(int row, int k) { return static_cast<uint32_t>((k >> 6) * kKBlock) + sw128(row, k & 63); }
 
+// Workspace position of the cluster-summed partial of column `col` (down
+// columns 0..R-1, then inject columns R..R+7) for row b of cluster p. With
+// one row, (p, b, col) row-major with NCP columns: dec_up_um pulls the whole
+// array with one bulk copy. With more rows (split mode, where up rank c
+// reduces the `per` down columns c*per.. and rank 0 the inject columns) the
+// down columns are grouped by the rank that consumes them, (p, rank, b,
+// per), followed by the inject columns as (p, b, 8): each rank pulls one
+// contiguous block per cluster and rank 0 one block of inject columns.
+__host__ __device__ inline int64_t part_index(bool split, int p, int b, int col, int B, int C, int R, int NCP, int per,
+                                              int NCLU) {
+  if (!split) return (static_cast<int64_t>(p) * B + b) * NCP + col;
+  if (col < R) {
+    const int rank = col / per;
+    return ((static_cast<int64_t>(p) * C + rank) * B + b) * per + (col - rank * per);
+  }
+  return static_cast<int64_t>(NCLU) * C * B * per + (static_cast<int64_t>(p) * B + b) * 8 + (col - R);
+}
+
 // --------------------------------------------------------------- dec_down --
 
 struct DownSmem {
@@ -95,8 +113,8 @@ struct DownArgs {
   const T *streams, *prev_out, *prev_gate, *ns, *wd, *wi;
   T* sout;
   float* inv_ws;   // (B, C)
-  float* part_ws;  // (NCLU, B, NCP), NCP = R + 8
-  int B, C, H, R, KS, CL, NCP;
+  float* part_ws;  // one row: (NCLU, B, NCP), NCP = R + 8; split: see part_index
+  int B, C, H, R, KS, CL, NCP, split, per, NCLU;
   float eps;
   int weights_static;
 };
@@ -218,7 +236,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
   float ssq[MB];
 #pragma unroll
   for (int b = 0; b < MB; ++b) ssq[b] = 0.0f;
-  constexpr int RB = MB < 2 ? MB : 2;  // rows whose loads are in flight together
+  constexpr int RB = MB < 4 ? MB : 4;  // rows whose loads are in flight together
   #pragma unroll 1
   for (int v = tid; v < NVr; v += nthr) {
     const int kk = v * VEC - hk0;
@@ -337,7 +355,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r < CL) t += x[r];
-    a.part_ws[(static_cast<int64_t>(cluster_id) * B + b) * NCP + c_lo + lc] = rok ? t : qnan;
+    a.part_ws[part_index(a.split != 0, cluster_id, b, c_lo + lc, B, C, R, NCP, a.per, a.NCLU)] = rok ? t : qnan;
   }
   tc_fence_before();
   __syncthreads();
@@ -506,19 +524,21 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   if (warp == 0) {
     uint32_t bytes;
     if (!split) bytes = static_cast<uint32_t>(NCLU * B * NCP * 4);
-    else bytes = static_cast<uint32_t>(NCLU * B * ncols * 4 + (do_post ? NCLU * B * 32 : 0));
+    else bytes = static_cast<uint32_t>(NCLU * B * a.per * 4 + (do_post ? NCLU * B * 32 : 0));
     if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     __syncwarp();
     if (!split) {
       if (lane == 0) bulk_g2s(st, a.part_ws, bytes, bar);
     } else {
+      // one block of B * per partials per cluster for this rank, and (rank 0
+      // of the first column tile) one block of every cluster's inject partials
       #pragma unroll 1
-      for (int i = lane; i < NCLU * B; i += 32) {
-        if (ncols > 0)
-          bulk_g2s(st + static_cast<size_t>(i) * a.per, a.part_ws + static_cast<int64_t>(i) * NCP + c * a.per,
-                   static_cast<uint32_t>(ncols * 4), bar);
-        if (do_post) bulk_g2s(st + inj_off + static_cast<size_t>(i) * 8, a.part_ws + static_cast<int64_t>(i) * NCP + R, 32u, bar);
-      }
+      for (int p = lane; p < NCLU; p += 32)
+        bulk_g2s(st + static_cast<size_t>(p) * B * a.per,
+                 a.part_ws + (static_cast<int64_t>(p) * C + c) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
+      if (do_post && lane == 0)
+        bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * C * B * a.per,
+                 static_cast<uint32_t>(NCLU * B * 32), bar);
     }
   }
   float inv_r[MB];
@@ -647,7 +667,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
 
 struct UmCfg {
   bool ok;
-  int KS, NSL, CL, NCLU, NCP, down_threads, up_threads;
+  int KS, NSL, CL, NCLU, NCP, R, down_threads, up_threads;
 };
 
 int cluster_for(int n) {
@@ -680,6 +700,7 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   if (H % kUpHS != 0 || H > 16384) return g;
   const int CH = C * H;
   g.NCP = R + 8;
+  g.R = R;
   g.down_threads = 12 * 32;  // a multiple of 4 warps (TMEM lane quarters)
   g.KS = 0;
   for (int ks = 16; ks <= H; ks += 16) {
@@ -706,7 +727,10 @@ Layout um_layout(int64_t rows, int C, const UmCfg& g) {
   Layout L;
   L.inv = 0;
   L.part = align_up(static_cast<size_t>(rows) * C * 4, 256);
-  L.total = align_up(L.part + static_cast<size_t>(g.NCLU) * rows * g.NCP * 4, 256);
+  const Stage sg = stage_for(rows, C, g.R, g.NCLU, g.NCP);
+  const size_t nf = sg.split ? static_cast<size_t>(g.NCLU) * rows * (static_cast<size_t>(C) * sg.per + 8)
+                             : static_cast<size_t>(g.NCLU) * rows * g.NCP;
+  L.total = align_up(L.part + nf * 4, 256);
   return L;
 }
 
@@ -728,7 +752,9 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g) {
   da.inv_ws = inv_ws;
   da.part_ws = part_ws;
   da.B = static_cast<int>(p.rows);
-  da.C = p.C; da.H = p.H; da.R = p.R; da.KS = g.KS; da.CL = g.CL; da.NCP = g.NCP;
+  da.C = p.C; da.H = p.H; da.R = p.R; da.KS = g.KS; da.CL = g.CL; da.NCP = g.NCP; da.NCLU = g.NCLU;
+  const Stage sg = stage_for(p.rows, p.C, p.R, g.NCLU, g.NCP);
+  da.split = sg.split; da.per = sg.per;
   da.eps = p.eps;
   da.weights_static = (p.flags & HC_FLAG_WEIGHTS_STATIC) ? 1 : 0;
   const size_t dsm = down_smem(MB, g.KS, p.R, p.C, g.CL, g.down_threads / 32).total;
@@ -737,7 +763,6 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g) {
   e = launch_pdl(dec_down_um<T, MB>, dim3(g.NSL), dim3(g.down_threads), dsm, p.stream, static_cast<unsigned>(g.CL), da);
   if (e != cudaSuccess) return e;
 
-  const Stage sg = stage_for(p.rows, p.C, p.R, g.NCLU, g.NCP);
   UpArgs<T> ua;
   ua.streams = da.streams;
   ua.prev_out = da.prev_out;
