@@ -68,6 +68,17 @@ def test_second_prefill_shape_decode_rows(hc, dt, rows):
     check(hc, rows, 8, 1280, 320, dt, expect_path=hc.HC_PATH_DECODE)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("rows", [2, 5])
+@pytest.mark.parametrize("shape", [(8, 1280, 200), (4, 1024, 104)], ids=lambda s: "C%d_H%d_R%d" % s)
+def test_decode_ranks_with_ragged_column_shares(hc, dt, rows, shape):
+    """Decode with two or more rows hands each up rank a share of ceil(R/C)
+    (rounded to 4) down columns; with these R the last rank's share is short
+    (4 and 20 columns): every column still reaches its consumer."""
+    C, H, R = shape
+    check(hc, rows, C, H, R, dt, seed=21, expect_path=hc.HC_PATH_DECODE)
+
+
 @pytest.mark.parametrize("attrs", [DEFAULT_ATTRS, ODD_ATTRS], ids=["default", "odd"])
 @pytest.mark.parametrize("dt", ["bf16", "f32"])
 def test_attributes(hc, attrs, dt):
