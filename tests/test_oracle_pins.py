@@ -342,6 +342,55 @@ def test_row_independence_and_thread_count(oracle_lib, dt):
             assert np.array_equal(a[j:j + 1], b)
 
 
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_overflowing_branch_acts_as_a_zero_branch(oracle_lib, dt):
+    """No prologue, epsilon > 0: a branch whose sum of squares overflows fp32
+    has mean = inf and inv = 1/sqrt(inf) = 0, so its hn is (signed) zero, the
+    same hn as a branch of zeros (inv = 1/sqrt(epsilon), hn = 0 * inv * ns).
+    Every later step sees the same values, so pre_output and post_gate keep
+    their bits (IEEE-754 inf and signed-zero arithmetic)."""
+    C, H, R = 4, 64, 16
+    d = I.make_block(3, C, H, R, dt, seed=14, prologue=False)
+    big = d["streams"].clone().view(3, C, H)
+    big[:, 2] = (big[:, 2].double() * 2.0 ** 100).to(TORCH_DT[dt])
+    zero = d["streams"].clone().view(3, C, H)
+    zero[:, 2] = 0
+    a = run_oracle(oracle_lib, dict(d, streams=big.view(3, C * H)), C, dt, I.QWEN_ATTRS, trace=True)
+    b = run_oracle(oracle_lib, dict(d, streams=zero.view(3, C * H)), C, dt, I.QWEN_ATTRS)
+    assert np.isfinite(codes_to_f64(a[0], dt)).all()
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    hn = oracle_lib.split_trace(a[3], C, H, R)["hn"].reshape(3, C, H)
+    assert np.all(hn[:, 2] == 0)
+
+
+@pytest.mark.parametrize("dt", ["f32", "f16", "bf16"])
+def test_nan_or_inf_input_poisons_only_its_row(oracle_lib, dt):
+    """A NaN in one branch of a row's streams makes that branch's RMS NaN; an
+    inf in prev_block_output makes S infinite in every branch, the RMS
+    infinite and hn = inf * 0 = NaN there. Either way every down column sums
+    a NaN, so the whole row's pre_output and post_gate are NaN, while
+    streams_out keeps S (NaN or inf only where the input was) and the other
+    rows keep the bits they have alone."""
+    C, H, R = 4, 64, 16
+    d = I.make_block(3, C, H, R, dt, seed=15, prologue=True)
+    st, po = d["streams"].clone(), d["prev_out"].clone()
+    st[1, 1 * H + 5] = float("nan")
+    po[2, 7] = float("inf")
+    pre, post, sout = run_oracle(oracle_lib, dict(d, streams=st, prev_out=po), C, dt, I.QWEN_ATTRS)
+    pre_f, post_f, sout_f = (codes_to_f64(x, dt) for x in (pre, post, sout))
+    assert np.isnan(pre_f[1:]).all() and np.isnan(post_f[1:]).all()
+    nan_at = np.zeros((3, C * H), bool)
+    nan_at[1, H + 5] = True
+    assert np.array_equal(np.isnan(sout_f), nan_at)
+    inf_at = np.zeros((3, C * H), bool)
+    inf_at[2, [c * H + 7 for c in range(C)]] = True
+    assert np.array_equal(np.isinf(sout_f), inf_at)
+    one = {k: (v[0:1] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+    alone = run_oracle(oracle_lib, one, C, dt, I.QWEN_ATTRS)
+    for x, y in zip((pre, post, sout), alone):
+        assert np.array_equal(x[0:1], y)
+
+
 def test_single_branch_reduces_to_rms_norm(oracle_lib):
     """C = 1, rho = 1, zero up weights: pre = hn / 2 with hn = RMSNorm(streams) *
     norm_scale, checked against torch's rms_norm in float64."""

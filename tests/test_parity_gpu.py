@@ -273,6 +273,44 @@ def test_cross_path_agreement(hc):
     assert (a[0] == b[0]).mean() > 0.8
 
 
+@pytest.mark.parametrize("rows,dt,flags", [(5, "bf16", 0), (5, "f16", 0), (5, "f32", 0), (130, "bf16", 0),
+                                            (130, "f16", 0), (5, "bf16", 2), (5, "f32", 2)],
+                         ids=["decode-bf16", "decode-f16", "decode-f32", "prefill-bf16", "prefill-f16",
+                              "general-bf16", "general-f32"])
+def test_special_values(hc, rows, dt, flags):
+    """IEEE special values on every path, against the oracle: a NaN in one
+    branch of row 1's streams and an inf in row 2's prev_out make those rows'
+    pre_output and post_gate NaN (streams_out keeps them only where they
+    entered); in row 3 (fp32 / bf16) one branch overflows its sum of squares,
+    so its inv is 0 and its hn zero, a finite result held to the usual
+    tolerance; the other rows are unaffected."""
+    C, H, R = 4, 2560, 320
+    d = I.make_block(rows, C, H, R, dt, seed=41, prologue=True)
+    d["streams"][1, 1 * H + 5] = float("nan")
+    d["prev_out"][2, 7] = float("inf")
+    if dt != "f16":
+        v = d["streams"].view(rows, C, H)
+        v[3, 2] = (v[3, 2].double() * 2.0 ** 100).to(TORCH_DT[dt])
+    path = {0: None, 2: hc.HC_PATH_GENERAL}[flags]
+    if path is not None:
+        assert hc.path(rows, C, H, R, TORCH_DT[dt], flags) == path
+    gpre, gpost, gsout = run_gpu(hc, d, C, I.QWEN_ATTRS, flags=flags)
+    opre, opost, osout, _ = run_oracle(d, C, dt, I.QWEN_ATTRS)
+    from _util import codes_to_f64
+    for g, o in ((gpre, opre), (gpost, opost)):
+        gn, on = np.isnan(codes_to_f64(g, dt)), np.isnan(codes_to_f64(o, dt))
+        assert np.array_equal(gn, on)
+        assert on[1:3].all() and not on[[0] + list(range(3, rows))].any()
+    gs, os_ = codes_to_f64(gsout, dt), codes_to_f64(osout, dt)
+    assert np.array_equal(np.isnan(gs), np.isnan(os_)) and np.isnan(os_).sum() == 1
+    fin = ~np.isnan(os_)
+    assert np.array_equal(gs[fin], os_[fin]) and np.isinf(os_).sum() == C
+    keep = torch.tensor([0] + list(range(3, rows)))
+    ref = run_oracle(d, C, dt, I.QWEN_ATTRS, rows_idx=keep)
+    k = keep.numpy()
+    compare((gpre[k], gpost[k], gsout[k]), ref, dt, C, H, R, I.QWEN_ATTRS, inputs=d)
+
+
 # ------------------------------------------------- prefill (tensor cores) --
 
 PREFILL_SHAPES = [(4, 2560, 320), (8, 1280, 320), (1, 4096, 64), (2, 128, 64), (8, 64, 128), (4, 256, 448),
