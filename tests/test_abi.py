@@ -86,3 +86,53 @@ def test_no_gpu_fails_loudly(L):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call() in (B.HC_ERR_CUDA, B.HC_ERR_UNSUPPORTED)
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "hc_lowrank_mix.h"
+#include "hc_row_ops.h"
+
+int main(void) {
+  hc_attrs_t a = hc_attrs_default();
+  char fake[64];
+  hc_status_t s;
+  if (a.silu_alpha != 1.0f || a.flags != 0u) return 1;
+  if (strcmp(hc_status_string(HC_ERR_WORKSPACE), "HC_ERR_WORKSPACE") != 0) return 2;
+  /* invalid sizes are refused on the host, before any device access */
+  s = hc_lowrank_mix(fake, fake, fake, fake, fake, NULL, NULL, -1, 4, 64, 16, &a, HC_BF16,
+                     fake, fake, NULL, NULL, 0, NULL);
+  if (s != HC_ERR_INVALID_ARG || hc_last_error()[0] == '\0') return 3;
+  /* zero rows launch nothing and need no row pointers */
+  s = hc_lowrank_mix(NULL, fake, fake, fake, fake, NULL, NULL, 0, 4, 64, 16, NULL, HC_F32,
+                     NULL, NULL, NULL, NULL, 0, NULL);
+  if (s != HC_OK) return 4;
+  if (hc_inv_rms(fake, 1, 0, 1e-6f, HC_F32, (float*)fake, NULL) != HC_ERR_INVALID_ARG) return 5;
+  if (hc_engram_gate(fake, fake, fake, fake, fake, 0, 4, 64, 1e-5f, HC_F16, fake, NULL) != HC_OK) return 6;
+  printf("ok %s\n", hc_status_string(HC_OK));
+  return 0;
+}
+"""
+
+
+def test_headers_serve_a_plain_c_program(L, tmp_path):
+    """include/*.h compile as strict C99 (no C++ or CUDA types in the
+    signatures), and a C program linked against the library gets the
+    documented host-side results (argument errors, zero rows) without a GPU."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "consumer.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "consumer"
+    lib_dir = os.path.dirname(B.LIB_PATH)
+    cmd = [cc, "-std=c99", "-pedantic", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+           str(src), "-o", str(exe), B.LIB_PATH, f"-Wl,-rpath,{lib_dir}"]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([str(exe)], capture_output=True, text=True, env=env, timeout=60)
+    assert r.returncode == 0 and r.stdout.strip() == "ok HC_OK", (r.returncode, r.stdout, r.stderr)
