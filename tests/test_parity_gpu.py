@@ -238,6 +238,29 @@ def test_guard_bands_untouched(hc):
         assert torch.all(wbuf[:8192] == 0xA5) and torch.all(wbuf[8192 + nws:] == 0xA5)
 
 
+@pytest.mark.parametrize("rows,dt,flags", [(1, "bf16", 0), (5, "bf16", 0), (5, "f32", 0), (300, "bf16", 0),
+                                            (600, "f16", 0), (5, "bf16", 2), (40, "f32", 2)],
+                         ids=["decode1", "decode5", "decode5-f32", "prefill300", "prefill600-f16", "general5",
+                              "general40-f32"])
+def test_workspace_poisoned_with_nan(hc, rows, dt, flags):
+    """Every path writes each workspace word before reading it: a workspace
+    filled with NaN bytes and one filled with zeros give bitwise the same
+    outputs (a read of stale scratch would carry the NaN into them)."""
+    C, H, R = 4, 2560, 320
+    d = I.make_block(rows, C, H, R, dt, seed=43, prologue=True)
+    g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
+    n = hc.workspace_size(rows, C, H, R, TORCH_DT[dt], flags)
+    outs = []
+    for fill in (0xFF, 0x00):
+        ws = torch.full((max(n, 1),), fill, dtype=torch.uint8, device="cuda")
+        outs.append(hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, workspace=ws, flags=flags,
+                                   **I.QWEN_ATTRS))
+        torch.cuda.synchronize()
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.uint8), b.view(torch.uint8))
+    assert not torch.isnan(outs[0][0].float()).any() and not torch.isnan(outs[0][1].float()).any()
+
+
 def test_misaligned_pointers_take_general_path(hc):
     C, H, R, rows = 4, 256, 32, 3
     d = I.make_block(rows, C, H, R, "bf16", seed=12, prologue=True)
