@@ -186,6 +186,46 @@ def test_two_chained_blocks(hc, dt):
     compare(g2, o2, dt, C, H, R, I.QWEN_ATTRS, check_streams_out=False, inputs=w2)
 
 
+def test_decode_chain_under_pdl_matches_oracle_block_by_block(hc):
+    """The 96-block decode chain as the benchmark launches it: rows 1, bf16,
+    96 distinct weight sets, every block enqueued back to back on one stream
+    with the weights-static flag and one shared workspace, so each block's
+    kernels start while the previous block's still run (programmatic
+    dependent launch). Every block keeps its outputs; block i is checked
+    against the oracle fed with the GPU's own inputs to block i (block i-1's
+    outputs), so a read of data the previous block had not yet written, or a
+    workspace reused too early, shows as a mismatch."""
+    C, H, R, rows, n = 4, 2560, 320, 1, 96
+    dev = torch.device("cuda")
+    flags = hc.HC_FLAG_WEIGHTS_STATIC
+    weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(n)]
+    a0 = I.make_activations(rows, C, H, "bf16", seed=0, block=0, prologue=True, device=dev)
+    pre = torch.empty(n, rows, H, dtype=torch.bfloat16, device=dev)
+    post = torch.empty(n, rows, C, dtype=torch.bfloat16, device=dev)
+    sout = torch.empty(n, rows, C * H, dtype=torch.bfloat16, device=dev)
+    work = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
+
+    def inputs_of(i):
+        if i == 0:
+            return a0["streams"], a0["prev_out"], a0["prev_gate"]
+        return sout[i - 1], pre[i - 1], post[i - 1]
+
+    for i in range(n):
+        st, po, pg = inputs_of(i)
+        w = weights[i]
+        hc.lowrank_mix(st, w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], po, pg, num_branches=C,
+                       flags=flags, out=(pre[i], post[i], sout[i]), workspace=work, **I.QWEN_ATTRS)
+    torch.cuda.synchronize()
+    assert torch.isfinite(pre.float()).all() and torch.isfinite(post.float()).all()
+    for i in range(n):
+        st, po, pg = inputs_of(i)
+        d = {k: v.cpu() for k, v in weights[i].items()}
+        d.update(streams=st.cpu(), prev_out=po.cpu(), prev_gate=pg.cpu())
+        ref = run_oracle(d, C, "bf16", I.QWEN_ATTRS)
+        gpu = (to_codes(pre[i]), to_codes(post[i]), to_codes(sout[i]))
+        compare(gpu, ref, "bf16", C, H, R, I.QWEN_ATTRS, inputs=d)
+
+
 @pytest.mark.parametrize("rows", [1, 8, 64])
 def test_cuda_graph_replay_bitwise_equal_to_eager(hc, rows):
     C, H, R = 4, 2560, 320
