@@ -18,7 +18,11 @@
  * (= down*SG = d), up, g, pre_output, inject, post_gate; the sigmoid is
  * 1/(1+expf(-x)) in fp32 with an IEEE divide. Accumulation order is fixed for a
  * given shape and path: results are bitwise deterministic, and a row's bits do
- * not depend on the number of rows within one path (see hc_lowrank_mix_path).
+ * not depend on the number of rows within one path (see hc_lowrank_mix_path);
+ * the prefill path splits its down projection differently up to 512 rows and
+ * beyond, so there the invariance holds within each of the two ranges. Across
+ * paths or ranges a row stays within the stated tolerance of the exact result
+ * but may differ in its last bits.
  *
  * Memory: every tensor argument is a DEVICE pointer to contiguous row-major
  * data of element type T (all tensors share T). The caller owns all memory;
