@@ -89,30 +89,6 @@ template <> struct SigmoidT<__half> {
 };
 template <typename T> __device__ __forceinline__ float sigmoid_rT(float x) { return SigmoidT<T>::eval(x); }
 
-// sigmoid(x) in fp32 to within a few ulps, branch-free and valid for every
-// x (infinities saturate, NaN propagates): e = 2^(-|x| log2 e) in (0, 1]
-// (Cody-Waite split of the argument, hardware ex2 approximation; |x| is
-// clamped at 128 in the correction term only), r = 1 / (1 + e) (hardware
-// reciprocal and one Newton step), sigmoid = r for x >= 0 and e * r below.
-// Used where the sigmoid dominates the cost (the prefill epilogue); after
-// rounding to T it can differ from sigmoid_acc's rounding only within a few
-// fp32 ulps of a rounding midpoint of T.
-__device__ __forceinline__ float sigmoid_fast(float x) {
-  const float kLog2e = 1.44269502f, kLog2eTail = 1.9259630e-08f, kLn2 = 0.69314718f;
-  const float ax = fabsf(x), axc = fminf(ax, 128.0f);
-  const float t_hi = __fmul_rn(ax, -kLog2e);
-  const float m = __fmul_rn(axc, kLog2e);
-  const float t_lo = fmaf(axc, -kLog2eTail, fmaf(axc, -kLog2e, m));
-  float p;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(p) : "f"(t_hi));
-  const float e = __fmul_rn(p, fmaf(t_lo, kLn2, 1.0f));
-  const float s = __fadd_rn(1.0f, e);
-  float r;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
-  r = fmaf(r, fmaf(-s, r, 1.0f), r);
-  return x >= 0.0f ? r : __fmul_rn(e, r);
-}
-
 // Prologue: S = rT(streams + gate * prev), multiply then add, each rounded.
 template <typename T> __device__ __forceinline__ float prologue_s(float s, float gate, float prev) {
   return rT<T>(__fadd_rn(s, __fmul_rn(gate, prev)));

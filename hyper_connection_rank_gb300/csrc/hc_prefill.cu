@@ -16,10 +16,10 @@
 //            inject likewise -> post_gate.
 //   pf_up    (tcgen05): up = d @ W_u for a tile of 128 rows x (C branches x
 //            64 features); the epilogue reads the accumulators from tensor
-//            memory and computes g = rT(sigmoid(rT(up))) (sigmoid_fast: the
-//            sigmoid evaluations dominate this kernel's instruction count),
-//            hn * g, the pre-mix over the branches in order and pre_output,
-//            all in registers.
+//            memory and computes g = rT(sigmoid(rT(up))) with exactly the bits
+//            of the accurate rounded sigmoid (a table in bf16, the checked
+//            fast form in fp16), hn * g, the pre-mix over the branches in
+//            order and pre_output, all in registers.
 //
 // Pipelines: one TMA thread, one MMA thread, four epilogue warps; stage
 // hand-off through mbarriers (all waits bounded, see hc_async.cuh).
@@ -168,12 +168,11 @@ pf_norm(const T* __restrict__ streams, const T* __restrict__ prev_out, const T* 
 struct PfDownArgs {
   CUtensorMap tm_a;        // hn tiles [row tiles * C*H/64][128][64], box {64 k, 128 rows, 1}
   CUtensorMap tm_b;        // down_w viewed as [R/64 column chunks][C*H rows][64 columns],
-                           // box {64 columns, 64 / cs rows, R/64 chunks}
+                           // box {64 columns, 64 rows, R/64 chunks}
   const uint16_t* wi;      // inject_w [C*H, C] (16-bit codes)
   float* part;             // [ksplit, rows, R + 16] fp32: down columns, then inject
   int rows, R, C, k_per_split, stages;
   int kblocks;             // C*H / 64: hn tiles per row tile
-  int cs;                  // cluster size along the row tiles (1, 2 or 4)
 };
 
 template <typename T>
@@ -207,48 +206,39 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Row tiles that share a K slice run as clusters of `cs` CTAs: the W_d slab
-// of a stage (64 K rows x R columns) is the same for all of them, so cluster
-// rank p loads K rows [p * 64/cs, (p+1) * 64/cs) of it once and multicasts
-// them to every CTA of the cluster; each CTA releases a stage to all of them
-// (commit multicast), so the empty barriers count cs arrivals. L2 delivers
-// the weights once per cluster instead of once per CTA.
+// Each CTA loads its own operands: per stage the A tile of its 128 hn rows
+// (one 3D copy of a contiguous 16 KB tile) and the W_d slab of the stage's 64
+// K rows (one 3D copy of all R/64 column chunks). Row tiles that share a K
+// slice read the same slab; L2 serves the repeats.
 //
 // Shared memory of a stage: the A tile (16 KB), then the B operand as
-// [part p < cs][chunk j <= R/64][64/cs K rows][128 bytes], chunk R/64 being
-// the inject columns. A stage's B operand for K rows [16 kk, 16 kk + 16) sits
-// in one part, so each MMA reads one part with chunk stride (64/cs) * 128.
+// [chunk j <= R/64][64 K rows][128 bytes], chunk R/64 being the inject
+// columns; each MMA reads its 16 K rows of every chunk with chunk stride 8 KB.
 template <bool BF16>
 __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__ PfDownArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int R = a.R, C = a.C, NB = R / 64, S = a.stages, NTOT = R + 16, NP = R + 16, CS = a.cs;
-  const int prow = kBK / CS;                                        // K rows per part
-  const uint32_t chunk_bytes = static_cast<uint32_t>(prow) * 128u;
-  const uint32_t part_bytes = static_cast<uint32_t>(NB + 1) * chunk_bytes;
-  const int stage_bytes = kATileBytes + (NB + 1) * kBoxBytes;     // A + CS parts
+  const int R = a.R, C = a.C, NB = R / 64, S = a.stages, NTOT = R + 16, NP = R + 16;
+  const uint32_t chunk_bytes = static_cast<uint32_t>(kBoxBytes);  // 64 K rows x 128 bytes
+  const int stage_bytes = kATileBytes + (NB + 1) * kBoxBytes;     // A, then R/64 + 1 chunks of B
   uint8_t* wi_s = smem + S * stage_bytes;                           // this CTA's K rows of inject_weight
   const uint32_t wi_bytes = static_cast<uint32_t>(a.k_per_split * C * 2);
   PipeBars* pb = reinterpret_cast<PipeBars*>(wi_s + ((wi_bytes + 15u) & ~15u));
-  const uint32_t rank = CS > 1 ? cluster_ctarank() : 0u;
-  const uint16_t mask = static_cast<uint16_t>((1u << CS) - 1u);
   const int m0 = blockIdx.x * kBM, ks = blockIdx.y;
   const int k_begin = ks * a.k_per_split, nk = a.k_per_split / kBK;
   const uint32_t ncols = NTOT <= 256 ? 256u : 512u;
 
-  // zero the inject chunk of every part of every stage once; only its first
-  // C columns change
-  for (int st = 0; st < S; ++st)
-    for (int p = 0; p < CS; ++p) {
-      uint4* z = reinterpret_cast<uint4*>(smem + st * stage_bytes + kATileBytes + p * part_bytes + NB * chunk_bytes);
-      for (uint32_t i = threadIdx.x; i < chunk_bytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
-    }
+  // zero the inject chunk of every stage once; only its first C columns change
+  for (int st = 0; st < S; ++st) {
+    uint4* z = reinterpret_cast<uint4*>(smem + st * stage_bytes + kATileBytes + NB * chunk_bytes);
+    for (uint32_t i = threadIdx.x; i < chunk_bytes / 16; i += blockDim.x) z[i] = make_uint4(0u, 0u, 0u, 0u);
+  }
   fence_proxy_async_smem();
   if (warp == 0 && lane == 0) {
     for (int st = 0; st < S; ++st) {
       mbar_init(&pb->full[st], 1);
-      mbar_init(&pb->empty[st], static_cast<uint32_t>(CS));
+      mbar_init(&pb->empty[st], 1);
     }
     mbar_init(&pb->done, 1);
     mbar_init(&pb->aux, 1);
@@ -263,8 +253,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA's barriers exist before any peer multicasts into it
-  if (CS > 1) cluster_sync_all();
   const uint32_t tmem = pb->tmem_base;
   // inject_weight is never written by the preceding kernel (weights): its
   // K slice may be copied before the dependency wait
@@ -292,8 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       fence_proxy_async_smem();
       for (int kr = lane; kr < kBK; kr += 32) {
         const uint16_t* src = reinterpret_cast<const uint16_t*>(wi_s) + static_cast<int64_t>(k - k_begin + kr) * C;
-        const int p = kr / prow, r = kr - p * prow;
-        uint8_t* dst = bsp + p * part_bytes + NB * chunk_bytes + r * 128 + ((r & 7) << 4);
+        uint8_t* dst = bsp + NB * chunk_bytes + kr * 128 + ((kr & 7) << 4);
         if (C == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
         else if (C == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
         else if (C == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
@@ -304,10 +291,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       if (lane == 0) {
         mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + NB * kBoxBytes));
         tma_load_3d(sp, &a.tm_a, 0, 0, blockIdx.x * a.kblocks + k / kBK, &pb->full[st]);
-        if (CS > 1)
-          tma_load_3d_mc(bsp + rank * part_bytes, &a.tm_b, 0, k + static_cast<int>(rank) * prow, 0, &pb->full[st], mask);
-        else
-          tma_load_3d(bsp, &a.tm_b, 0, k, 0, &pb->full[st]);
+        tma_load_3d(bsp, &a.tm_b, 0, k, 0, &pb->full[st]);
       }
     }
   } else if (warp == 1) {
@@ -324,10 +308,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
       const uint64_t ad0 = smem_desc_sw128(s0, 16, 1024);
       uint64_t bd[kBK / 16];
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk) {
-        const int p = (kk * 16) / prow, r0 = kk * 16 - p * prow;
-        bd[kk] = smem_desc_sw128(s0 + kATileBytes + p * part_bytes + r0 * 128, chunk_bytes, 1024);
-      }
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        bd[kk] = smem_desc_sw128(s0 + kATileBytes + kk * 16 * 128, chunk_bytes, 1024);
       const uint64_t n1_off = static_cast<uint64_t>((4u * chunk_bytes) >> 4);  // chunk 4 = column 256
       for (int it = 0; it < nk && ok; ++it) {
         const int st = it % S;
@@ -342,14 +324,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
           mma_f16(tmem, adesc, bd[kk] + so, id0, acc);
           if (N1 > 0) mma_f16(tmem + 256, adesc, bd[kk] + so + n1_off, id1, acc);
         }
-        if (CS > 1) mma_commit_mc(&pb->empty[st], mask);
-        else mma_commit(&pb->empty[st]);
+        mma_commit(&pb->empty[st]);
       }
       mma_commit(&pb->done);
     }
   } else {
     // Epilogue: accumulators -> shared memory (the pipeline stages are idle:
-    // every stage, the peers' multicasts included, has been consumed), then
+    // every stage has been consumed), then
     // whole rows to global memory with coalesced 16-byte stores.
     ok = mbar_wait(&pb->done, 0, &g_pf_wait_timeouts);
     tc_fence_after();
@@ -396,8 +377,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
     tc_fence_after();
     tmem_dealloc(tmem, ncols);
   }
-  // no CTA leaves while a peer may still multicast into it or arrive on it
-  if (CS > 1) cluster_sync_all();
 }
 
 // down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
@@ -496,8 +475,10 @@ __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __res
 // NaN); a sign bit moved to bit 11 selects the negative half of the table. The
 // table holds bf16 values and hn * g + acc is one mixed-precision fused
 // multiply-add (bf16 operands, fp32 addend): no operand is widened first. fp16
-// keeps the branch-free fast sigmoid (its rounding can differ in one ulp near
-// a rounding midpoint).
+// (whose non-constant range is too wide for a table in shared memory) uses
+// sigmoid_rT, the fast sigmoid that falls back to the accurate form near a
+// rounding midpoint of T: the same bits as the accurate rounded sigmoid on
+// every fp16 input.
 constexpr int kUpEpiWarps = 16;
 constexpr int kUpHnWarp = 2 + kUpEpiWarps;                 // the warp that loads hn
 constexpr int kUpThreads = 32 * (kUpHnWarp + 1);
@@ -735,11 +716,14 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
             float hf[16];
             V8<T>::unpack(v0, hf);
             V8<T>::unpack(v1, hf + 8);
-            // hn * g is exact in fp32 (two 16-bit significands), so the fused
-            // multiply-add gives the bits of the separate multiply and add
+            // g = rT(sigmoid(u)) bit for bit as the accurate form rounds it
+            // (sigmoid_rT: fast evaluation, the accurate one near a rounding
+            // midpoint of T); hn * g is exact in fp32 (two 16-bit
+            // significands), so the fused multiply-add gives the bits of the
+            // separate multiply and add
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              acc[j] = fmaf(hf[j], rT<T>(sigmoid_fast(rT<T>(__uint_as_float(up[j])))), acc[j]);
+              acc[j] = fmaf(hf[j], sigmoid_rT<T>(rT<T>(__uint_as_float(up[j]))), acc[j]);
           }
           // the slot is released only after every lane has used what it read
           // from it, and each lane first orders its (generic-proxy) reads
@@ -909,11 +893,8 @@ cudaError_t run_prefill(const Problem& p) {
   const unsigned mtiles = static_cast<unsigned>((rows + kBM - 1) / kBM);
   PfDownArgs da;
   const uint64_t hn_tiles = static_cast<uint64_t>(mtiles) * (CH / 64);
-  // row tiles that share a K slice go in pairs (clusters of 2) once there are two
-  const int cs = mtiles >= 2 ? 2 : 1;
-  if (!make_tile_map(&da.tm_a, hn, BF16, hn_tiles) || !make_chunk_map(&da.tm_b, p.down_w, BF16, R, CH, kBK / cs))
+  if (!make_tile_map(&da.tm_a, hn, BF16, hn_tiles) || !make_chunk_map(&da.tm_b, p.down_w, BF16, R, CH, kBK))
     return cudaErrorInvalidValue;
-  da.cs = cs;
   da.wi = static_cast<const uint16_t*>(p.inject_w);
   da.part = part;
   da.rows = static_cast<int>(rows);
@@ -928,8 +909,7 @@ cudaError_t run_prefill(const Problem& p) {
   const size_t dsm = 1024 + static_cast<size_t>(da.stages) * dstage + wi_stage + sizeof(PipeBars);
   e = ensure_smem<pf_down<BF16>>(dsm);
   if (e != cudaSuccess) return e;
-  const unsigned gx = (mtiles + cs - 1) / cs * cs;  // a padded tile loads zeros (out of range) and stores nothing
-  e = launch_pdl(pf_down<BF16>, dim3(gx, ksplit), dim3(kTcThreads), dsm, p.stream, static_cast<unsigned>(cs), da);
+  e = launch_pdl(pf_down<BF16>, dim3(mtiles, ksplit), dim3(kTcThreads), dsm, p.stream, 1u, da);
   if (e != cudaSuccess) return e;
 
   const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};

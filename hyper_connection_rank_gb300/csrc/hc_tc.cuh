@@ -79,16 +79,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-// Arrive once on `bar` (same shared-memory offset) in every CTA of the
-// cluster named by `cta_mask` when every MMA issued so far is done.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_addr(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
 // Warp-collective load of 16 consecutive fp32 columns of the 32 lanes the
 // warp may access (lane = row): thread t gets row (lane base + t). The load
 // and its wait are one asm statement: tcgen05.ld writes its registers
@@ -143,17 +133,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
           smem_addr(dst)),
       "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
-      : "memory");
-}
-
-// The same box delivered to the same shared-memory offset, and completed on
-// the same mbarrier offset, in every CTA of the cluster named by `cta_mask`.
-__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar)), "h"(cta_mask)
       : "memory");
 }
 
