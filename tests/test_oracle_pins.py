@@ -32,6 +32,16 @@ import torch.nn.functional as F
 from _util import DT_CODE, TORCH_DT, codes_to_f64, from_codes, to_codes, ulp_diff
 from hyper_connection_rank_gb300 import inputs as I
 
+
+@pytest.fixture(autouse=True, params=["cpu", pytest.param("gpu-session", marks=pytest.mark.gpu)])
+def session(request):
+    """Every pin runs twice: in the CPU test session and again, marked gpu, in
+    the session that runs beside the GPU tests on the host processor of the
+    machine that holds the GPU. The checker that judges the GPU results is
+    then pinned on that host's architecture (aarch64 there, x86-64 here) and
+    compiler, not only on the one it was written on."""
+    return request.param
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 KEYS = ("streams", "norm_scale", "down_w", "up_w", "inject_w", "prev_out", "prev_gate")
 UNIT_ROUNDOFF = {"f32": 2.0 ** -24, "f16": 2.0 ** -11, "bf16": 2.0 ** -8}

@@ -27,6 +27,16 @@ from hyper_connection_rank_gb300 import inputs as I
 scipy_special = pytest.importorskip("scipy.special")
 
 
+@pytest.fixture(autouse=True, params=["cpu", pytest.param("gpu-session", marks=pytest.mark.gpu)])
+def session(request):
+    """Every pin runs twice: in the CPU test session and again, marked gpu, in
+    the session that runs beside the GPU tests on the host processor of the
+    machine that holds the GPU. The checker that judges the GPU results is
+    then pinned on that host's architecture (aarch64 there, x86-64 here) and
+    compiler, not only on the one it was written on."""
+    return request.param
+
+
 @pytest.fixture(scope="module")
 def oracle():
     import oracle as O

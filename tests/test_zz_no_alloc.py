@@ -5,9 +5,10 @@ block: a host whose memory pool owns the whole GPU, a plug-in interface that
 hands over tensors and a stream but no allocator, or code inside a strict
 stream capture. hc_lowrank_mix_decode_noalloc serves them by keeping its
 scratch in a fixed array inside the library. These tests call it twice in a
-row and check both results against hc_lowrank_mix (which takes a workspace
-from the caller), within the tolerance of the parity tests, and check that
-problems too large for the array are refused with a clear error.
+row and check both results bit for bit against hc_lowrank_mix (which takes a
+workspace from the caller and runs the same kernels in the same order) and
+against the CPU oracle within the tolerance of the parity tests, and check
+that problems too large for the array are refused with a clear error.
 """
 import ctypes
 
@@ -15,7 +16,8 @@ import numpy as np
 import pytest
 import torch
 
-from _util import to_codes, ulp_diff
+from _parity import compare, run_oracle
+from _util import to_codes
 from hyper_connection_rank_gb300 import inputs as I
 
 pytestmark = pytest.mark.gpu
@@ -51,9 +53,10 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(api):
     hc, B, f = api
     C, H, R = 4, 2560, 320
     cases = [(8, 31), (1, 32)]          # a larger call, then a smaller one over the same scratch
-    blocks, outs = [], []
+    blocks, outs, hosts = [], [], []
     for rows, seed in cases:
         d = I.make_block(rows, C, H, R, "bf16", seed=seed, prologue=True)
+        hosts.append(d)
         g = {k: (v.cuda() if v is not None else None) for k, v in d.items()}
         out = (torch.empty(rows, H, dtype=torch.bfloat16, device="cuda"),
                torch.empty(rows, C, dtype=torch.bfloat16, device="cuda"),
@@ -64,12 +67,13 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(api):
         status = call_noalloc(B, f, g, rows, C, H, R, out, I.QWEN_ATTRS)
         assert status == 0, B.lib().hc_last_error().decode()
     torch.cuda.synchronize()
-    for (rows, _), g, out in zip(cases, blocks, outs):
+    for (rows, _), g, out, d in zip(cases, blocks, outs, hosts):
         ref = hc.lowrank_mix(*[g[k] for k in KEYS], num_branches=C, **I.QWEN_ATTRS)
         torch.cuda.synchronize()
-        assert torch.equal(out[2].view(torch.int16), ref[2].view(torch.int16))
-        assert ulp_diff(to_codes(out[0]), to_codes(ref[0]), "bf16").max() <= 2
-        assert ulp_diff(to_codes(out[1]), to_codes(ref[1]), "bf16").max() <= 2
+        for a, b in zip(out, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        compare(tuple(to_codes(t) for t in out), run_oracle(d, C, "bf16", I.QWEN_ATTRS), "bf16", C, H, R,
+                I.QWEN_ATTRS, inputs=d)
 
 
 def test_refuses_problems_beyond_the_static_scratch(api):
