@@ -197,7 +197,7 @@ def run_ours(args, rank, world, local_rank):
     for i in range(W):
         step(i)
     torch.cuda.synchronize()
-    g_full = capture(NSETS) if K >= NSETS else None
+    g_full = capture(NSETS)
     g_rem = capture(K % NSETS) if K % NSETS else None
     torch.cuda.synchronize()
 
@@ -206,6 +206,10 @@ def run_ours(args, rank, world, local_rank):
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     barrier()
     torch.cuda.synchronize()
+    # untimed lead-in: one 96-block replay enqueued ahead of the timed one, so
+    # the timed blocks start right behind running work (steady state) and no
+    # graph-launch gap enters the timed region, whatever K is
+    g_full.replay()
     ev0.record(stream)
     for _ in range(K // NSETS):
         g_full.replay()
@@ -233,6 +237,8 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16", "data": "synthetic (seeded splitmix64 + Box-Muller; Qwen-shaped, random weights)",
         "config": {"workload": WORKLOAD, "rows": rows, "C": C, "H": H, "R": R, "weight_sets": NSETS,
                    "l2": "inputs larger than L2: 96 weight sets of 13.2 MB rotated (1.27 GB)",
+                   "timed_region": "K chained blocks (graph replays) enqueued right behind an untimed 96-block "
+                                   "lead-in replay: steady state at any K, no graph-launch gap timed",
                    "parallelism": f"replicas x{world}"},
         "us_per_block": round(us_per_block, 4),
         "roofline": {"bound": "hbm", "kernel": "decode block (dec_down + dec_up, PDL-overlapped)",
@@ -249,8 +255,54 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0 and not args.no_sweep:
         del weights
         torch.cuda.empty_cache()
+        result["isolated"] = isolated_latency(hc, I, dev, pk)
         result["sweep"] = sweep(hc, I, dev, pk)
     return result
+
+
+def isolated_latency(hc, I, dev, pk, reps=200):
+    """One decode block at a time with L2 cold: before each call a reduction
+    reads a 512 MB buffer (four times L2; reading leaves no dirty lines to be
+    written back during the call), then the call alone is timed with events on
+    its stream. Min and median over `reps` calls, for rows 1/2/4/8 in bf16
+    and fp16 (the single-block and row-sweep configurations, measured one
+    call at a time rather than as a chain)."""
+    import torch
+    flags = hc.HC_FLAG_WEIGHTS_STATIC
+    flush = torch.ones(256 << 20, dtype=torch.float16, device=dev)
+    out = {}
+    for dt, tdt in (("bf16", torch.bfloat16), ("f16", torch.float16)):
+        w = I.make_weights(C, H, R, dt, seed=0, block=0, device=dev)
+        for rows in (1, 2, 4, 8):
+            a = I.make_activations(rows, C, H, dt, seed=0, block=0, prologue=True, device=dev)
+            o = (torch.empty(rows, H, dtype=tdt, device=dev), torch.empty(rows, C, dtype=tdt, device=dev),
+                 torch.empty(rows, C * H, dtype=tdt, device=dev))
+            ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, tdt, flags)), dtype=torch.uint8, device=dev)
+
+            def call():
+                hc.lowrank_mix(a["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], a["prev_out"],
+                               a["prev_gate"], num_branches=C, flags=flags, out=o, workspace=ws, **QWEN)
+
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            s = torch.cuda.current_stream(dev)
+            ts = []
+            for _ in range(reps):
+                flush.sum()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(s)
+                call()
+                e1.record(s)
+                e1.synchronize()
+                ts.append(1000.0 * e0.elapsed_time(e1))
+            b = block_bytes(rows, C, H, R, 2)
+            t = min(ts)
+            out[f"decode_rows{rows}_{dt}"] = {"us": round(t, 3), "us_median": round(statistics.median(ts), 3),
+                                              "hbm_frac": round(b / (t * 1e-6) / 1e9 / pk["hbm"], 4)}
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def profile_case(args, hc, I, dev, rows, flags):
@@ -375,34 +427,100 @@ def e2e_measure(args, hc, I, weights, dev, flags):
             "api": "hc_lowrank_mix (C ABI, through ctypes) with host buffers: one pinned H2D copy, the block, one D2H copy per step; eager launches"}
 
 
+def host_cpu():
+    """Host processor as the benchmark saw it: logical cores, architecture
+    and model name (from lscpu, else /proc/cpuinfo)."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() in ("Model name", "Model"):
+                model = line.split(":", 1)[1].strip()
+                if line.startswith("Model name"):
+                    break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"nproc": os.cpu_count(), "machine": platform.machine(), "model": model}
+
+
+def _oracle_rate(run, seconds, min_calls=2):
+    """Calls of run() until about `seconds` have passed: (calls, elapsed)."""
+    n, t0 = 0, time.perf_counter()
+    while True:
+        run(n)
+        n += 1
+        el = time.perf_counter() - t0
+        if (el >= seconds and n >= min_calls) or n >= 100000:
+            return n, el
+
+
 def cpu_baseline(seconds):
-    """The oracle, as it stands, on a bounded sample of the workload: chained
-    rows=1 bf16 blocks over 2 weight sets, single-threaded (one row cannot be
-    split across threads by the oracle), for about `seconds` of CPU time."""
+    """The oracle, as it stands, on bounded samples of the benchmark's
+    configurations, on the host cores of this machine.
+
+    Headline (the line's own workload, single-threaded: the oracle splits a
+    call across threads by rows, and a chain of one-row blocks has one row per
+    call): chained rows=1 bf16 decode blocks over 2 weight sets for about
+    `seconds`. Then on all host cores: nproc independent one-row chains as one
+    nproc-row call per block (the oracle's row threads), and a sample of rows
+    of each 8192-row prefill block (C=4, H=2560 bf16; C=8, H=1280 fp16), one
+    thread and all threads. Rates are rows/s."""
     import numpy as np
     import torch
 
     import oracle
     from hyper_connection_rank_gb300 import inputs as I
     oracle.build()
+    info = host_cpu()
+    ncores = max(1, int(info["nproc"] or 1))
     codes = lambda t: None if t is None else t.contiguous().view(torch.int16).numpy().view(np.uint16)
-    ws = [I.make_weights(C, H, R, "bf16", seed=0, block=i) for i in range(2)]
-    ws = [{k: codes(v) for k, v in w.items()} for w in ws]
-    act = {k: codes(v) for k, v in I.make_activations(1, C, H, "bf16", seed=0, block=0, prologue=True).items()}
-    n, t0 = 0, time.perf_counter()
-    while True:
-        w = ws[n % 2]
-        pre, post, sout = oracle.lowrank_mix(act["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
-                                             act["prev_out"], act["prev_gate"], num_branches=C,
-                                             dtype=oracle.DT_BF16, nthreads=1, **QWEN)
-        act = {"streams": sout, "prev_out": pre, "prev_gate": post}
-        n += 1
-        el = time.perf_counter() - t0
-        if (el >= seconds and n >= 3) or n >= 100000:
-            break
-    return {"value": round(n / el, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} chained decode blocks (rows=1, bf16, C=4, H=2560, R=320) over 2 weight sets, "
-                      f"{el:.1f} s on 1 host thread", "us_per_block": round(1e6 * el / n, 1)}
+
+    def chain(rows, nthreads, secs):
+        ws = [{k: codes(v) for k, v in I.make_weights(C, H, R, "bf16", seed=0, block=i).items()} for i in range(2)]
+        act = [{k: codes(v) for k, v in I.make_activations(rows, C, H, "bf16", seed=0, block=0,
+                                                          prologue=True).items()}]
+
+        def one(n):
+            w, a = ws[n % 2], act[0]
+            pre, post, sout = oracle.lowrank_mix(a["streams"], w["norm_scale"], w["down_w"], w["up_w"],
+                                                 w["inject_w"], a["prev_out"], a["prev_gate"], num_branches=C,
+                                                 dtype=oracle.DT_BF16, nthreads=nthreads, **QWEN)
+            act[0] = {"streams": sout, "prev_out": pre, "prev_gate": post}
+        return _oracle_rate(one, secs, min_calls=3)
+
+    n, el = chain(1, 1, seconds)
+    res = {"value": round(n / el, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
+           "sample": f"{n} chained decode blocks (rows=1, bf16, C=4, H=2560, R=320) over 2 weight sets, "
+                     f"{el:.1f} s on 1 host thread", "us_per_block": round(1e6 * el / n, 1), "host": info}
+    lines = {}
+    n, el = chain(ncores, ncores, seconds / 2)
+    lines["decode_rows1_chain_bf16"] = {
+        "rows_per_s": round(n * ncores / el, 2), "threads": ncores,
+        "sample": f"{ncores} independent one-row chains as {n} calls of {ncores} rows ({el:.1f} s)"}
+    for dt, Cp, Hp in (("bf16", 4, 2560), ("f16", 8, 1280)):
+        code = {"bf16": oracle.DT_BF16, "f16": oracle.DT_F16}[dt]
+        w = {k: codes(v) for k, v in I.make_weights(Cp, Hp, R, dt, seed=0, block=0).items()}
+        full = I.make_block(max(4 * ncores, 8), Cp, Hp, R, dt, seed=0, prologue=True)
+        for threads, rows in ((1, 4), (ncores, 4 * ncores)):
+            a = {k: codes(full[k][:rows]) for k in ("streams", "prev_out", "prev_gate")}
+
+            def one(_n, a=a, threads=threads):
+                oracle.lowrank_mix(a["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"],
+                                   a["prev_out"], a["prev_gate"], num_branches=Cp, dtype=code, nthreads=threads,
+                                   **QWEN)
+            n, el = _oracle_rate(one, seconds / 4, min_calls=1)
+            lines[f"prefill_rows8192_C{Cp}_H{Hp}_{dt}_{'1thread' if threads == 1 else 'all_cores'}"] = {
+                "rows_per_s": round(n * rows / el, 2), "threads": threads,
+                "us_per_8192_row_block": round(1e6 * el / (n * rows) * 8192, 1),
+                "sample": f"{n} calls of {rows} rows of the 8192-row block ({el:.1f} s)"}
+    res["other_configs"] = lines
+    return res
 
 
 def sweep(hc, I, dev, pk):
@@ -621,7 +739,8 @@ def run_reference(args, rank, world):
             "data": "synthetic", "config": {"workload": WORKLOAD.replace("graph replay", "CPU oracle, 2 weight sets"),
                                             "rows": 1, "C": C, "H": H, "R": R},
             "cpu_baseline": {"value": round(v, 2), "unit": "rows/s", "cores": 1, "kind": "oracle",
-                             "sample": f"{n} chained decode blocks on 1 host thread ({el:.1f} s)"},
+                             "sample": f"{n} chained decode blocks on 1 host thread ({el:.1f} s)",
+                             "host": host_cpu()},
             "e2e": {"value": round(v, 2), "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
