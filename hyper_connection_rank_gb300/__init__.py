@@ -7,10 +7,10 @@ and must have been built (``hyper_connection_rank_gb300.build.build()``).
 """
 from ._binding import (HC_FLAG_FORCE_GENERAL, HC_FLAG_WEIGHTS_STATIC, HC_PATH_DECODE, HC_PATH_GENERAL,
                        HC_PATH_NONE, HC_PATH_PREFILL, PATH_NAMES, HcError, attrs_default, debug_sigmoid_exact,
-                       debug_sigmoid_table, debug_wait_timeouts, engram_gate, inv_rms, load_library, lowrank_mix, path,
+                       debug_sigmoid_table, debug_sigmoid_table_f16, debug_wait_timeout, debug_wait_timeouts, engram_gate, inv_rms, load_library, lowrank_mix, path,
                        workspace_size)
 
 __all__ = ["lowrank_mix", "inv_rms", "engram_gate", "path", "workspace_size", "attrs_default", "load_library", "debug_wait_timeouts",
-           "debug_sigmoid_exact", "debug_sigmoid_table",
+           "debug_wait_timeout", "debug_sigmoid_exact", "debug_sigmoid_table_f16", "debug_sigmoid_table",
            "HcError", "HC_FLAG_WEIGHTS_STATIC", "HC_FLAG_FORCE_GENERAL", "HC_PATH_NONE", "HC_PATH_DECODE",
            "HC_PATH_PREFILL", "HC_PATH_GENERAL", "PATH_NAMES"]

@@ -28,7 +28,8 @@ DTYPE_CODES = {torch.float32: HC_F32, torch.float16: HC_F16, torch.bfloat16: HC_
 # Every symbol include/hc_lowrank_mix.h declares.
 EXPORTS = ("hc_attrs_default", "hc_lowrank_mix_path", "hc_lowrank_mix_workspace_size", "hc_lowrank_mix",
            "hc_status_string", "hc_last_error", "hc_debug_wait_timeouts", "hc_debug_sigmoid_exact",
-           "hc_debug_sigmoid_table", "hc_inv_rms", "hc_engram_gate")
+           "hc_debug_sigmoid_table", "hc_debug_sigmoid_table_f16", "hc_debug_sigmoid_table_f16_bytes", "hc_debug_wait_timeout", "hc_debug_phase_clocks", "hc_debug_sync_probe", "hc_lowrank_mix_decode_noalloc", "hc_inv_rms",
+           "hc_engram_gate")
 
 
 class HcAttrs(ctypes.Structure):
@@ -72,6 +73,15 @@ def load_library(path: str = LIB_PATH):
         L.hc_debug_sigmoid_exact.restype = ci
         L.hc_debug_sigmoid_table.argtypes = [vp, vp]
         L.hc_debug_sigmoid_table.restype = ci
+        L.hc_debug_sigmoid_table_f16_bytes.restype = sz
+        L.hc_debug_sigmoid_table_f16.argtypes = [vp, vp, sz, vp]
+        L.hc_debug_sigmoid_table_f16.restype = ci
+        L.hc_debug_wait_timeout.argtypes = [vp, ctypes.c_longlong, vp]
+        L.hc_debug_wait_timeout.restype = ci
+        L.hc_debug_phase_clocks.argtypes = [vp, sz]
+        L.hc_debug_phase_clocks.restype = sz
+        L.hc_debug_sync_probe.argtypes = [ci, ci, ci, sz, vp, sz, vp]
+        L.hc_debug_sync_probe.restype = ci
         f32 = ctypes.c_float
         L.hc_inv_rms.argtypes = [vp, i64, i64, f32, ci, vp, vp]
         L.hc_inv_rms.restype = ci
@@ -176,6 +186,15 @@ def debug_wait_timeouts(reset: bool = False) -> int:
     return lib().hc_debug_wait_timeouts(1 if reset else 0)
 
 
+def debug_wait_timeout(limit_cycles: int = 2_000_000, device="cuda"):
+    """Run the bounded-wait give-up check (hc_debug_wait_timeout): returns the
+    32 floats the probe kernel wrote (NaN where its wait gave up)."""
+    out = torch.zeros(32, dtype=torch.float32, device=device)
+    s = torch.cuda.current_stream(out.device)
+    check(lib().hc_debug_wait_timeout(_ptr(out), int(limit_cycles), s.cuda_stream))
+    return out
+
+
 def debug_sigmoid_exact(dt: torch.dtype, device="cuda"):
     """(fast, accurate) T codes of rT(sigmoid(x)) for all 65536 codes x of dt
     (float16 or bfloat16), as int16 tensors on `device` (see
@@ -185,6 +204,18 @@ def debug_sigmoid_exact(dt: torch.dtype, device="cuda"):
     s = torch.cuda.current_stream(fast.device)
     check(lib().hc_debug_sigmoid_exact(DTYPE_CODES[dt], _ptr(fast), _ptr(acc), s.cuda_stream))
     return fast, acc
+
+
+def debug_sigmoid_table_f16(device="cuda"):
+    """g for every fp16 code through the fp16 prefill epilogue's table lookup,
+    as a float32 tensor on `device` (see hc_debug_sigmoid_table_f16)."""
+    L = lib()
+    g = torch.empty(65536, dtype=torch.float32, device=device)
+    n = L.hc_debug_sigmoid_table_f16_bytes()
+    table = torch.empty(n, dtype=torch.uint8, device=device)
+    s = torch.cuda.current_stream(g.device)
+    check(L.hc_debug_sigmoid_table_f16(_ptr(g), _ptr(table), n, s.cuda_stream))
+    return g
 
 
 def debug_sigmoid_table(device="cuda"):

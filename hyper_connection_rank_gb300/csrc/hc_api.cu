@@ -240,6 +240,46 @@ hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_o
   return HC_OK;
 }
 
+size_t hc_debug_phase_clocks(void* buf, size_t bytes) { return hc::set_phase_clocks(buf, bytes); }
+
+hc_status_t hc_debug_sync_probe(int mode, int ctas, int rounds, size_t smem_bytes, void* scratch,
+                                size_t scratch_bytes, struct CUstream_st* stream) {
+  if (mode < 0 || mode > 2) return hc::set_error(HC_ERR_INVALID_ARG, "mode must be 0, 1 or 2");
+  if (ctas < 1 || ctas > 1024 || rounds < 1 || rounds > 100000)
+    return hc::set_error(HC_ERR_INVALID_ARG, "ctas must lie in [1, 1024] and rounds in [1, 100000]");
+  if (smem_bytes > 200 * 1024) return hc::set_error(HC_ERR_INVALID_ARG, "smem_bytes above 200 KB");
+  if (scratch == nullptr || scratch_bytes < (32u + static_cast<size_t>(ctas)) * 4u ||
+      (reinterpret_cast<uintptr_t>(scratch) & 15u) != 0)
+    return hc::set_error(HC_ERR_WORKSPACE, "scratch must hold (32 + ctas) 32-bit words, 16-byte aligned");
+  int num_sms = 0;
+  const hc_status_t ds = device_info(&num_sms);
+  if (ds != HC_OK) return ds;
+  const cudaError_t e = hc::launch_sync_probe(mode, ctas, rounds, smem_bytes, static_cast<unsigned int*>(scratch),
+                                              reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(HC_ERR_CUDA, "launch: %s", cudaGetErrorString(e));
+  return HC_OK;
+}
+
+hc_status_t hc_debug_wait_timeout(float* out, long long limit_cycles, struct CUstream_st* stream) {
+  if (out == nullptr) return hc::set_error(HC_ERR_INVALID_ARG, "null output pointer");
+  if (limit_cycles < 1000 || limit_cycles > 4000000000LL)
+    return hc::set_error(HC_ERR_INVALID_ARG, "limit_cycles must lie in [1e3, 4e9]");
+  const cudaError_t e = hc::launch_wait_timeout_probe(out, limit_cycles, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return hc::set_error(HC_ERR_CUDA, cudaGetErrorString(e));
+  return HC_OK;
+}
+
+size_t hc_debug_sigmoid_table_f16_bytes(void) { return hc::sigmoid_table16_bytes(); }
+
+hc_status_t hc_debug_sigmoid_table_f16(float* g_out, void* table, size_t table_bytes, struct CUstream_st* stream) {
+  if (g_out == nullptr || table == nullptr) return hc::set_error(HC_ERR_INVALID_ARG, "null pointer");
+  if (table_bytes < hc::sigmoid_table16_bytes() || (reinterpret_cast<uintptr_t>(table) & 15u) != 0)
+    return hc::set_error(HC_ERR_WORKSPACE, "table buffer too small or not 16-byte aligned");
+  const cudaError_t e = hc::launch_sigmoid_table16_codes(table, g_out, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return hc::set_error(HC_ERR_CUDA, cudaGetErrorString(e));
+  return HC_OK;
+}
+
 hc_status_t hc_debug_sigmoid_table(float* g_out, struct CUstream_st* stream) {
   if (g_out == nullptr) return hc::set_error(HC_ERR_INVALID_ARG, "null output pointer");
   const cudaError_t e = hc::launch_sigmoid_table_codes(g_out, reinterpret_cast<cudaStream_t>(stream));

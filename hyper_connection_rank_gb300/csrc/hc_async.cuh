@@ -57,17 +57,26 @@ __device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity to complete.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* timeouts) {
+// Wait for the phase with the given parity to complete, for at most
+// `limit_cycles` SM clock cycles; on giving up, count it in `timeouts` and
+// return false.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t* bar, uint32_t parity, unsigned int* timeouts,
+                                                long long limit_cycles) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
     if (mbar_try(bar, parity)) return true;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit_cycles) {
       if (timeouts != nullptr) atomicAdd(timeouts, 1u);
       return false;
     }
   }
+}
+
+// Bounded wait for the phase with the given parity to complete (the limit
+// every kernel of the library uses).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned int* timeouts) {
+  return mbar_wait_limit(bar, parity, timeouts, kWaitLimitCycles);
 }
 
 // Plain arrive (count 1) on an mbarrier.
@@ -85,6 +94,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Prefetch `bytes` (a multiple of 16; address 16-byte aligned) from global
+// memory into L2, asynchronously and without a destination.
+__device__ __forceinline__ void l2_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (bypasses L1), grouped by
 // commit_group / wait_group.
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
@@ -92,6 +107,8 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most the most recently committed group is still in flight.
+__device__ __forceinline__ void cp_async_wait_group1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // Cluster barrier halves. Every CTA of a cluster arrives early (relaxed: no
 // memory ordering) and waits just before its first store into a peer's

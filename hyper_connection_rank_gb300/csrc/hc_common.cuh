@@ -52,9 +52,12 @@ static __device__ __noinline__ float sigmoid_acc(float x) {
 // reciprocal approximations and one Newton step for the reciprocal. Measured
 // over 2^30 points in [-40, 40] it stays within 6 fp32 ulps of sigmoid_acc, so
 // rounding it to T gives the same result unless it lies within a few ulps of
-// a rounding midpoint of T; there (within 24 ulps), in T's subnormal range,
-// for |x| > 80 (including infinities) and for NaN the accurate form is
-// evaluated instead.
+// a rounding midpoint of T; there (within kSigWindow = 8 ulps), in T's
+// subnormal range, for |x| > 80 (including infinities) and for NaN the
+// accurate form is evaluated instead. Its inputs are values of T, so the claim
+// is checked on every one of them (hc_debug_sigmoid_exact). The narrower the
+// window, the fewer warps take the accurate branch (in the prefill epilogue
+// that branch, not the fast form, set the cost of the fp16 gate).
 __device__ __forceinline__ float sigmoid_fast_f32(float x) {
   const float kLog2e = 1.44269502f, kLog2eTail = 1.9259630e-08f, kLn2 = 0.69314718f;
   const float nx = -x;
@@ -67,6 +70,7 @@ __device__ __forceinline__ float sigmoid_fast_f32(float x) {
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(s));
   return fmaf(r, fmaf(-s, r, 1.0f), r);
 }
+constexpr int kSigWindow = 8;
 template <typename T> struct SigmoidT;
 template <> struct SigmoidT<float> {
   static __device__ __forceinline__ float eval(float x) { return sigmoid_acc(x); }
@@ -75,7 +79,7 @@ template <> struct SigmoidT<__nv_bfloat16> {
   static __device__ __forceinline__ float eval(float x) {
     const float f = sigmoid_fast_f32(x);
     const int lo = static_cast<int>(__float_as_uint(f) & 0xFFFFu) - 0x8000;
-    const bool slow = (lo < 24 && lo > -24) || !(x >= -80.0f && x <= 80.0f);
+    const bool slow = (lo < kSigWindow && lo > -kSigWindow) || !(x >= -80.0f && x <= 80.0f);
     return Ty<__nv_bfloat16>::to_f(Ty<__nv_bfloat16>::from_f(slow ? sigmoid_acc(x) : f));
   }
 };
@@ -83,7 +87,7 @@ template <> struct SigmoidT<__half> {
   static __device__ __forceinline__ float eval(float x) {
     const float f = sigmoid_fast_f32(x);
     const int lo = static_cast<int>(__float_as_uint(f) & 0x1FFFu) - 0x1000;
-    const bool slow = (lo < 24 && lo > -24) || !(x >= -80.0f && x <= 80.0f) || f < 6.103515625e-05f;
+    const bool slow = (lo < kSigWindow && lo > -kSigWindow) || !(x >= -80.0f && x <= 80.0f) || f < 6.103515625e-05f;
     return Ty<__half>::to_f(Ty<__half>::from_f(slow ? sigmoid_acc(x) : f));
   }
 };
@@ -94,10 +98,14 @@ template <typename T> __device__ __forceinline__ float prologue_s(float s, float
   return rT<T>(__fadd_rn(s, __fmul_rn(gate, prev)));
 }
 
-// RMS statistic: inv = 1 / sqrt(sum / H + eps), correctly rounded steps.
-static __device__ __noinline__ float inv_rms(float sumsq, int H, float eps) {
-  float mean = __fdiv_rn(sumsq, static_cast<float>(H));
-  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+// RMS statistic: inv = 1 / sqrt(sum / H + eps), correctly rounded steps. The
+// last step is the correctly rounded reciprocal, which is the correctly
+// rounded quotient 1 / y for every y (infinities, zeros and NaN included),
+// with a shorter instruction sequence than the general divide; it sits on
+// the decode kernels' critical path.
+__device__ __forceinline__ float inv_rms(float sumsq, int H, float eps) {
+  const float mean = __fdiv_rn(sumsq, static_cast<float>(H));
+  return __frcp_rn(__fsqrt_rn(__fadd_rn(mean, eps)));
 }
 
 // hn = rT((S * inv) * norm_scale).

@@ -23,7 +23,9 @@
 //     the C inject columns sit at columns R..R+C-1 (in the padding of the
 //     last tile). Partial sums go to the rank that owns each 32-column group,
 //     by st.async into its shared memory, then in rank order to the workspace.
-//   dec_up_um: HS = 128 columns of branch c per CTA (one M tile).
+//   dec_up_um: one M tile of 128 output columns per CTA: F = 128 / C
+//     features of every branch, so the pre-mix over the branches sums in the
+//     CTA's own shared memory.
 #include <algorithm>
 #include <cooperative_groups.h>
 #include <type_traits>
@@ -45,7 +47,7 @@ namespace {
 
 constexpr int kUmRowsN = 16;    // MMA N: activation rows, padded
 constexpr int kUmMaxMT = 4;     // dec_down: at most 4 tiles of 128 columns (R + 8 <= 512)
-constexpr int kUpHS = 128;      // dec_up: columns per CTA (one M tile)
+constexpr int kUpHS = 128;      // dec_up: output columns per CTA (one M tile: C branches x 128/C features)
 constexpr int kUpIssuers = 4;   // dec_up: issuing warps = accumulators
 constexpr int kKBlock = 2048;   // one 64-k block of B: 16 rows x 128 bytes
 constexpr size_t kUmDownCap = 120 * 1024, kUmUpCap = 150 * 1024;
@@ -85,6 +87,27 @@ __host__ __device__ inline int64_t part_index(bool split, int p, int b, int col,
   return static_cast<int64_t>(NCLU) * C * B * per + (static_cast<int64_t>(p) * B + b) * 8 + (col - R);
 }
 
+// Phase clocks (diagnostic, hc_debug_phase_clocks): in the TIMED variants
+// thread 0 of every CTA records (%globaltimer in ns, clock64 in SM cycles) at
+// fixed points of the kernel into rec[CTA][point][2]. Thread 0 takes part in
+// every CTA-wide barrier and wait, so its stamps mark when the CTA as a whole
+// passed each point.
+constexpr int kPhasePoints = 10;
+constexpr int kPhaseMaxCtas = 256;
+__device__ __forceinline__ void phase_stamp(unsigned long long* rec, int point) {
+  unsigned long long gt;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(gt)::"memory");
+  const unsigned long long ck = static_cast<unsigned long long>(clock64());
+  rec[(blockIdx.x * kPhasePoints + point) * 2] = gt;
+  rec[(blockIdx.x * kPhasePoints + point) * 2 + 1] = ck;
+}
+#define HC_PHASE(point)                                        \
+  do {                                                         \
+    if constexpr (TIMED) {                                     \
+      if (threadIdx.x == 0) phase_stamp(a.phase, (point));     \
+    }                                                          \
+  } while (0)
+
 // --------------------------------------------------------------- dec_down --
 
 struct DownSmem {
@@ -99,8 +122,8 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
   L.b = a1024(L.a + 2 * MT * KS * 128);
   L.wis = a16(L.b + ceil_div(KS, 64) * kKBlock);
   L.ns = a16(L.wis + KS * C * 2);
-  L.ss = a16(L.ns + KS * 4);
-  L.wsum = a16(L.ss + MB * KS * 4);
+  L.ss = a16(L.ns + KS * 2);       // norm_scale of the slice, T
+  L.wsum = a16(L.ss + MB * KS * 2);  // S of the slice, T (already rounded to T: exact)
   L.inv = a16(L.wsum + nwarps * MB * 4);
   L.recv = a16(L.inv + MB * 4);
   L.bars = a16(L.recv + CL * MB * TPR * 32 * 4);
@@ -110,6 +133,7 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
 
 template <typename T>
 struct DownArgs {
+  CUtensorMap tm_wd;  // down_w [C*H rows, R columns], box {64 columns, KS rows}, 128-byte swizzle
   const T *streams, *prev_out, *prev_gate, *ns, *wd, *wi;
   T* sout;
   float* inv_ws;   // (B, C)
@@ -117,6 +141,9 @@ struct DownArgs {
   int B, C, H, R, KS, CL, NCP, split, per, NCLU;
   float eps;
   int weights_static;
+  const T* wu;                 // up_w: each CTA prefetches wu_prefetch_bytes of it into L2
+  uint32_t wu_prefetch_bytes;  // a multiple of 16; 0 = no prefetch
+  unsigned long long* phase;  // TIMED variants only: [CTA][kPhasePoints][2]
 };
 
 template <typename T>
@@ -128,8 +155,12 @@ __device__ __forceinline__ uint32_t idesc_t() {
 // beside it (measured: without the cap the 2-8 row variants take more
 // registers and the two kernels of a block stop overlapping under PDL,
 // costing 5-6 us per block).
-template <typename T, int MB>
-__global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
+// Phase points (TIMED): 0 entry, 1 weights issued (before the dependency
+// wait), 2 wait returned, 3 S pass done, 4 inverse RMS ready, 5 weights
+// landed, 6 MMA operands ready, 7 MMA done, 8 cluster exchange landed,
+// 9 partial sums written.
+template <typename T, int MB, bool TIMED = false>
+__global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int VEC = 8;
@@ -141,14 +172,15 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
   uint8_t* sA = smem + L.a;
   uint8_t* sB = smem + L.b;
   const T* wis = reinterpret_cast<const T*>(smem + L.wis);
-  float* ns_s = reinterpret_cast<float*>(smem + L.ns);
-  float* ss = reinterpret_cast<float*>(smem + L.ss);
+  T* ns_s = reinterpret_cast<T*>(smem + L.ns);
+  T* ss = reinterpret_cast<T*>(smem + L.ss);
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
   float* inv_s = reinterpret_cast<float*>(smem + L.inv);
   float* recv_s = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mma_bar = rbar + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 2);
+  uint64_t* wbar = rbar + 2;  // the slice's weights and norm_scale landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 3);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -161,10 +193,14 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
   const int c_lo = rank * OC, ncol = max(0, min(NCP, c_lo + OC) - c_lo);
   // inject columns R..R+C-1: box R/64, 16-byte chunk (R%64)/8
   const int ibox = R / 64, ich = (R % 64) / 8;
+  const int nbt = ceil_div(R, 64);  // boxes the W_d copies fill (a ragged last one with zeros)
+  HC_PHASE(0);
 
   if (tid == 0) {
     mbar_init(rbar, 1);
     mbar_init(mma_bar, MT);  // one commit per tile's issuing warp
+    mbar_init(wbar, 1);
+    tma_prefetch_desc(&a.tm_wd);
     mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(CL * ncol * B * 4));
     fence_mbar_init();
   }
@@ -173,60 +209,57 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     tmem_relinquish();
   }
   cluster_arrive_relaxed();
-  // zero B (rows >= B and k >= KS stay zero) and the A chunks no copy writes:
-  // box ibox from chunk ich on, and every later box
+  // zero B (rows >= B and k >= KS stay zero) and the A boxes no copy writes
+  // (every box from nbt on; the copies fill the columns of a ragged last box
+  // past R with zeros)
   #pragma unroll 1
   for (int i = tid; i < ceil_div(KS, 64) * kKBlock / 16; i += nthr) reinterpret_cast<uint4*>(sB)[i] = make_uint4(0, 0, 0, 0);
   #pragma unroll 1
-  for (int i = tid; i < (2 * MT - ibox) * KS * 8; i += nthr) {
-    const int bx = ibox + i / (KS * 8), rem = i - (bx - ibox) * KS * 8, r = rem >> 3, ch = rem & 7;
-    if (bx > ibox || ch >= ich)
-      *reinterpret_cast<uint4*>(sA + bx * boxb + r * 128 + ((ch ^ (r & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-  }
+  for (int i = tid; i < (2 * MT - nbt) * KS * 8; i += nthr)
+    reinterpret_cast<uint4*>(sA + nbt * boxb)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // weights: 16-byte chunks of each K row into their swizzled positions; warp
-  // 0 also copies the inject slice and, once it lands, places it in column R..
+  // weights, by one thread: the slice's KS rows of W_d as nbt tensor copies of
+  // 64 columns (each lands as one 128-byte-swizzled box of A), its rows of
+  // W_i and of norm_scale as two bulk copies, all completing on wbar; once
+  // they land warp 0 places the inject values in column R.. of A
   auto issue_weights = [&]() {
-    const int cpr = R / 8;
-    const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wd + static_cast<int64_t>(k0) * R);
-    #pragma unroll 1
-    for (int i = tid; i < KS * cpr; i += nthr) {
-      const int r = i / cpr, q = i - r * cpr;
-      cp_async16(sA + (q >> 3) * boxb + r * 128 + (((q & 7) ^ (r & 7)) << 4), gsrc + static_cast<size_t>(r) * R * 2 + q * 16);
-    }
-    if (warp == 0) {
-      const unsigned char* isrc = reinterpret_cast<const unsigned char*>(a.wi + static_cast<int64_t>(k0) * C);
-      #pragma unroll 1
-      for (int i = lane; i < KS * C * 2 / 16; i += 32) cp_async16(smem + L.wis + i * 16, isrc + i * 16);
-    }
-    cp_async_commit();
-    #pragma unroll 1
-    for (int i = tid; i < KS / VEC; i += nthr) {
-      float f[VEC];
-      V8<T>::unpack(ld16(a.ns + k0 + i * VEC), f);
-#pragma unroll
-      for (int j = 0; j < VEC; ++j) ns_s[i * VEC + j] = f[j];
+    if (tid == 0) {
+      const uint32_t ib = static_cast<uint32_t>(KS * C * 2), nb = static_cast<uint32_t>(KS * 2);
+      mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(nbt * boxb) + ib + nb);
+      for (int j = 0; j < nbt; ++j) tma_load_2d(sA + j * boxb, &a.tm_wd, j * 64, k0, wbar);
+      bulk_g2s(smem + L.wis, a.wi + static_cast<int64_t>(k0) * C, ib, wbar);
+      bulk_g2s(ns_s, a.ns + k0, nb, wbar);
+      // this CTA's share of the up weights into L2, for dec_up_um, whose
+      // CTAs start only after this kernel's dependency wait: the up weights
+      // then stream from HBM while this kernel runs, and dec_up_um's copies
+      // hit L2 (a prefetch changes no data; L2 is the point of coherence)
+      if (a.wu_prefetch_bytes != 0)
+        l2_prefetch(reinterpret_cast<const uint8_t*>(a.wu) + static_cast<size_t>(slice) * a.wu_prefetch_bytes,
+                    a.wu_prefetch_bytes);
     }
   };
+  // one thread per K row copies the row's C inject values (C * 2 bytes, at
+  // the start of a 16-byte chunk since R % 8 == 0) into column R.. of A
   auto place_inject = [&]() {
-    cp_async_wait_all();
-    __syncwarp();
-    #pragma unroll 1
-    for (int i = lane; i < KS * C; i += 32) {
-      const int r = i / C, cc = i - r * C;
-      *reinterpret_cast<T*>(sA + ibox * boxb + r * 128 + ((ich ^ (r & 7)) << 4) + cc * 2) = wis[r * C + cc];
+    if (tid < KS) {
+      const int r = tid;
+      uint8_t* dst = sA + ibox * boxb + r * 128 + ((ich ^ (r & 7)) << 4);
+      const T* src = wis + r * C;
+      if (C == 8) *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+      else if (C == 4) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+      else if (C == 2) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+      else *reinterpret_cast<T*>(dst) = *src;
     }
-    __syncwarp();
   };
-  if (a.weights_static) {
-    issue_weights();
-    if (warp == 0) place_inject();
-  }
+  // With static weights the copies start before the dependency wait.
+  if (a.weights_static) issue_weights();
+  HC_PHASE(1);
   pdl_wait();
+  HC_PHASE(2);
   if (!a.weights_static) issue_weights();
   pdl_trigger();
 
@@ -270,9 +303,9 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
 #pragma unroll
           for (int j = 0; j < VEC; ++j) ssq[b] = fmaf(sf[j], sf[j], ssq[b]);
           if (mine) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) ss[b * KS + kk + j] = sf[j];
-            if (a.sout != nullptr) st16(a.sout + b * CH + k0 + kk, pro ? V8<T>::pack(sf) : sv[bi]);
+            const uint4 sv_t = pro ? V8<T>::pack(sf) : sv[bi];  // S as T (each value already rounded)
+            *reinterpret_cast<uint4*>(ss + b * KS + kk) = sv_t;
+            if (a.sout != nullptr) st16(a.sout + b * CH + k0 + kk, sv_t);
           }
         }
     }
@@ -283,6 +316,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     if (lane == 0) wsum[warp * MB + b] = w;
   }
   __syncthreads();
+  HC_PHASE(3);
   if (tid < B) {
     float t = 0.0f;
     for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + tid];
@@ -291,16 +325,20 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     if (hk0 == 0) a.inv_ws[tid * C + c] = iv;
   }
   __syncthreads();
+  HC_PHASE(4);
+  const bool wok = mbar_wait(wbar, 0, &g_um_wait_timeouts);
+  HC_PHASE(5);
   // hn of the slice as T, into B at its swizzled position
   #pragma unroll 1
   for (int i = tid; i < B * KS; i += nthr) {
     const int b = i / KS, kk = i - b * KS;
-    *reinterpret_cast<T*>(sB + b_off(b, kk)) = Ty<T>::from_f(norm_hn<T>(ss[i], inv_s[b], ns_s[kk]));
+    *reinterpret_cast<T*>(sB + b_off(b, kk)) =
+        Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(ss[i]), inv_s[b], Ty<T>::to_f(ns_s[kk])));
   }
-  if (!a.weights_static && warp == 0) place_inject();
-  cp_async_wait_all();
+  place_inject();
   fence_proxy_async_smem();  // generic-proxy writes of A and B, visible to the tensor core
   __syncthreads();
+  HC_PHASE(6);
 
   // ---- [down | inject]^T = A * hn^T: tile mt (KS/16 k-steps) issued by
   // lane 0 of warp mt ----
@@ -315,8 +353,9 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     }
     mma_commit(mma_bar);
   }
-  const bool ok = mbar_wait(mma_bar, 0, &g_um_wait_timeouts);
+  const bool ok = mbar_wait(mma_bar, 0, &g_um_wait_timeouts) && wok;
   tc_fence_after();
+  HC_PHASE(7);
 
   // ---- each warp reads 32-column groups p = (tile p/4, lane quarter p%4)
   // with p % 4 == warp % 4 (a warp reaches only its own lane quarter) and
@@ -342,6 +381,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
     }
   }
   const bool rok = mbar_wait(rbar, 0, &g_um_wait_timeouts);
+  HC_PHASE(8);
 
   // ---- sum the received partials of the owned columns in rank order ----
   const int cluster_id = slice / CL;
@@ -359,6 +399,7 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
   }
   tc_fence_before();
   __syncthreads();
+  HC_PHASE(9);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 64);
@@ -368,18 +409,19 @@ __global__ void __maxnreg__(64) dec_down_um(const DownArgs<T> a) {
 // ----------------------------------------------------------------- dec_up --
 
 struct UpSmem {
-  uint32_t a, b, st, hn, ns, mix, bars, total;
+  uint32_t a, b, st, hn, ns, inv, mix, bars, total;
 };
 __host__ __device__ inline UpSmem up_smem(int MB, int R, int C, int st_bytes) {
-  const int R16 = (R + 15) / 16 * 16, HSc = kUpHS / C;
+  const int R16 = (R + 15) / 16 * 16;
   UpSmem L;
   L.a = 0;
   L.b = a1024(L.a + 2 * R16 * 128);
   L.st = a16(L.b + ceil_div(R16, 64) * kKBlock);
-  L.hn = a16(L.st + st_bytes);
-  L.ns = a16(L.hn + MB * kUpHS * 4);
-  L.mix = a16(L.ns + kUpHS * 4);
-  L.bars = a16(L.mix + C * MB * HSc * 4);
+  L.hn = a16(L.st + st_bytes);        // S, then hn, of the tile: T (both already rounded to T)
+  L.ns = a16(L.hn + MB * kUpHS * 2);  // norm_scale of the tile, T
+  L.inv = a16(L.ns + kUpHS * 2);      // inverse RMS of every (row, branch)
+  L.mix = a16(L.inv + MB * C * 4);    // hn * g of every (row, tile column)
+  L.bars = a16(L.mix + MB * kUpHS * 4);
   L.total = L.bars + 48 + 1024;
   return L;
 }
@@ -392,16 +434,19 @@ struct UpArgs {
   T *pre, *post;
   int B, C, H, R, NCLU, NCP, split, per, st_bytes;
   Attrs at;
+  unsigned long long* phase;  // TIMED variants only: [CTA][kPhasePoints][2]
 };
 
 // post_gate for every row: the inject partials summed in cluster order. One
-// CTA runs it; kept out of line so that the others never fetch its code.
+// CTA runs it, on its last warp (the one with the least of the d work, none
+// at one row), so that it stays off the path of the threads that feed the
+// MMA; kept out of line so that the other CTAs never fetch its code.
 template <typename T>
 __device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool split, int B, int C, int NCLU, int NCP,
                                            int R, bool ok, T* post, float gate_div, float gate_mul) {
   const float qnan = __int_as_float(0x7fc00000);
   #pragma unroll 1
-  for (int i = threadIdx.x; i < B * C; i += blockDim.x) {
+  for (int i = static_cast<int>(threadIdx.x) - static_cast<int>(blockDim.x - 32); i >= 0 && i < B * C; i += 32) {
     const int b = i / C, cc = i - b * C;
     const float* src = split ? st + inj_off + static_cast<size_t>(b) * 8 + cc : st + static_cast<size_t>(b) * NCP + R + cc;
     const size_t stride = split ? static_cast<size_t>(B) * 8 : static_cast<size_t>(B) * NCP;
@@ -410,45 +455,54 @@ __device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool
   }
 }
 
-template <typename T, int MB>
+// Phase points (TIMED): 0 entry, 1 prefetches issued (before the dependency
+// wait), 2 wait returned, 3 partial sums landed, 4 MMA operands ready, 5 MMA
+// done, 6 pre-mix products landed, 7 pre_output written.
+template <typename T, int MB, bool TIMED = false>
 __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int VEC = 8, HS = kUpHS;
   const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.B, C = a.C, H = a.H, R = a.R, NCLU = a.NCLU, NCP = a.NCP;
-  const int R16 = (R + 15) / 16 * 16, HSc = HS / C, boxb = R16 * 128;
+  const int R16 = (R + 15) / 16 * 16, F = HS / C, boxb = R16 * 128;
+  const int lgF = 31 - __clz(F);  // F = 128 / C is a power of two
   const UpSmem L = up_smem(MB, R, C, a.st_bytes);
   uint8_t* sA = smem + L.a;
   uint8_t* sB = smem + L.b;
   float* st = reinterpret_cast<float*>(smem + L.st);
-  float* hn_s = reinterpret_cast<float*>(smem + L.hn);
-  float* ns_s = reinterpret_cast<float*>(smem + L.ns);
+  T* hn_s = reinterpret_cast<T*>(smem + L.hn);
+  T* ns_s = reinterpret_cast<T*>(smem + L.ns);
+  float* inv_s = reinterpret_cast<float*>(smem + L.inv);
   float* mix_s = reinterpret_cast<float*>(smem + L.mix);
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + L.bars);  // partial sums landed
   uint64_t* dbar = bar + 1;                                     // d from every rank landed (split mode)
-  uint64_t* mbar = bar + 2;                                     // pre-mix products landed
   uint64_t* mma_bar = bar + 3;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
 
+  // Tile column m (= TMEM lane, = row of A) is feature f0 + m % F of branch
+  // m / F, f0 = blockIdx.x * F. With two or more rows, C consecutive CTAs
+  // form a cluster in which rank p reduces share p of the down columns and
+  // broadcasts its part of d (split mode); one row needs no cluster.
   cg::cluster_group cluster = cg::this_cluster();
-  const int c = static_cast<int>(cluster.block_rank());
-  const int q = blockIdx.x / C;
-  const int h0 = q * HS;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int f0 = blockIdx.x * F;
   const int64_t CH = static_cast<int64_t>(C) * H;
-  const int64_t col0 = static_cast<int64_t>(c) * H + h0;
   const bool pro = a.prev_out != nullptr;
-  const bool do_post = (q == 0 && c == 0);
+  const bool do_post = blockIdx.x == 0;
   // one row needs no split (the host never sets it then): the code is left out
   const bool split = MB > 1 && a.split != 0;
+  HC_PHASE(0);
+  // The next block's dec_down_um reads nothing before its own dependency wait
+  // but static weights (HC_FLAG_WEIGHTS_STATIC), and writes nothing before it:
+  // it may launch now and stream its weights during this kernel.
+  pdl_trigger();
 
   if (tid == 0) {
     mbar_init(bar, 1);
     mbar_init(dbar, 1);
-    mbar_init(mbar, 1);
     mbar_init(mma_bar, min(kUpIssuers, (R + 15) / 16));  // one commit per issuing warp
     mbar_arrive_expect_tx(dbar, split ? static_cast<uint32_t>(R * B * 2) : 0u);
-    mbar_arrive_expect_tx(mbar, C > 1 ? static_cast<uint32_t>(C * HSc * B * 4) : 0u);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -458,15 +512,23 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   cluster_arrive_relaxed();
   // The up weights and the block inputs are never written by the preceding
   // dec_down_um, which triggers its dependents only after its own wait:
-  // reading them before griddepcontrol.wait is safe. A: 16 chunks of 16 bytes
-  // per K row (two boxes of 64 columns), at their swizzled positions.
+  // reading them before griddepcontrol.wait is safe. norm_scale of the tile
+  // first, in a copy group of its own (the hn step waits for it alone); then
+  // A: 16 chunks of 16 bytes per K row (two boxes of 64 columns), at their
+  // swizzled positions; chunk qd holds tile columns 8 qd .. 8 qd + 7, i.e.
+  // features of branch 8 qd / F.
+  #pragma unroll 1
+  for (int i = tid; i < HS / VEC; i += nthr) {
+    const int m0 = i * VEC, cb = m0 >> lgF;
+    cp_async16(ns_s + m0, a.ns + static_cast<int64_t>(cb) * H + f0 + (m0 - (cb << lgF)));
+  }
+  cp_async_commit();
   {
-    const unsigned char* gsrc = reinterpret_cast<const unsigned char*>(a.wu + col0);
     #pragma unroll 1
     for (int i = tid; i < R * 16; i += nthr) {
-      const int r = i >> 4, qd = i & 15;
+      const int r = i >> 4, qd = i & 15, m0 = qd * 8, cb = m0 >> lgF;
       cp_async16(sA + (qd >> 3) * boxb + r * 128 + (((qd & 7) ^ (r & 7)) << 4),
-                 gsrc + (static_cast<int64_t>(r) * CH) * 2 + qd * 16);
+                 a.wu + static_cast<int64_t>(r) * CH + static_cast<int64_t>(cb) * H + f0 + (m0 - (cb << lgF)));
     }
     cp_async_commit();
     #pragma unroll 1
@@ -490,36 +552,30 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   const int nvh = HS / VEC;
   #pragma unroll 1
   for (int i = tid; i < B * nvh; i += nthr) {
-    const int b = i / nvh, qv = i - b * nvh;
-    float sf[VEC];
-    V8<T>::unpack(ld16(a.streams + b * CH + col0 + qv * VEC), sf);
+    const int b = i / nvh, m0 = (i - b * nvh) * VEC, cb = m0 >> lgF, f = f0 + (m0 - (cb << lgF));
+    uint4 sv = ld16(a.streams + b * CH + static_cast<int64_t>(cb) * H + f);
     if (pro) {
-      float pf[VEC];
-      V8<T>::unpack(ld16(a.prev_out + static_cast<int64_t>(b) * H + h0 + qv * VEC), pf);
-      const float gt = ldf(a.prev_gate + b * C + c);
+      float sf[VEC], pf[VEC];
+      V8<T>::unpack(sv, sf);
+      V8<T>::unpack(ld16(a.prev_out + static_cast<int64_t>(b) * H + f), pf);
+      const float gt = ldf(a.prev_gate + b * C + cb);
 #pragma unroll
       for (int j = 0; j < VEC; ++j) sf[j] = prologue_s<T>(sf[j], gt, pf[j]);
+      sv = V8<T>::pack(sf);
     }
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) hn_s[b * HS + qv * VEC + j] = sf[j];
-  }
-  #pragma unroll 1
-  for (int i = tid; i < nvh; i += nthr) {
-    float f[VEC];
-    V8<T>::unpack(ld16(a.ns + col0 + i * VEC), f);
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) ns_s[i * VEC + j] = f[j];
+    *reinterpret_cast<uint4*>(hn_s + b * HS + m0) = sv;
   }
   tc_fence_before();
+  HC_PHASE(1);
   pdl_wait();
-  pdl_trigger();
   cluster_wait();
   __syncthreads();  // barriers, TMEM address, S, ns and the zeroed regions visible CTA-wide
   tc_fence_after();
+  HC_PHASE(2);
   const uint32_t tmem = *tmem_slot;
 
   // ---- pull the down partials into shared memory ----
-  const int ncols = split ? max(0, min(R, (c + 1) * a.per) - c * a.per) : 0;
+  const int ncols = split ? max(0, min(R, (rank + 1) * a.per) - rank * a.per) : 0;
   const size_t inj_off = static_cast<size_t>(NCLU) * B * a.per;  // floats (split layout)
   if (warp == 0) {
     uint32_t bytes;
@@ -535,23 +591,29 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       #pragma unroll 1
       for (int p = lane; p < NCLU; p += 32)
         bulk_g2s(st + static_cast<size_t>(p) * B * a.per,
-                 a.part_ws + (static_cast<int64_t>(p) * C + c) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
+                 a.part_ws + (static_cast<int64_t>(p) * C + rank) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
       if (do_post && lane == 0)
         bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * C * B * a.per,
                  static_cast<uint32_t>(NCLU * B * 32), bar);
     }
   }
-  float inv_r[MB];
-#pragma unroll
-  for (int b = 0; b < MB; ++b) inv_r[b] = b < B ? a.inv_ws[b * C + c] : 0.0f;
+  // the inverse RMS of every (row, branch), from dec_down_um, while the
+  // partial sums travel
+  for (int i = tid; i < B * C; i += nthr) inv_s[i] = a.inv_ws[i];
   const bool ok = mbar_wait(bar, 0, &g_um_wait_timeouts);
+  cp_async_wait_group1();  // this thread's norm_scale chunk landed (the W_u copies may still fly)
+  __syncthreads();
   const float qnan = __int_as_float(0x7fc00000);
+  HC_PHASE(3);
 
-  // ---- d = ScaledSiLU(rT(sum of the partials in cluster order)) as T, into B ----
+  // ---- d = ScaledSiLU(rT(sum of the partials in cluster order)) as T, into B,
+  // on every warp but the last, which computes the post gate meanwhile ----
+  const int nthr_d = nthr - 32;
+  const bool d_thread = tid < nthr_d;
   if (!split) {
     const size_t stride = static_cast<size_t>(B) * NCP;
     #pragma unroll 1
-    for (int i = tid; i < B * R; i += nthr) {
+    for (int i = d_thread ? tid : B * R; i < B * R; i += nthr_d) {
       const int b = i / R, col = i - b * R;
       const float* src = st + static_cast<size_t>(b) * NCP + col;
       const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
@@ -562,7 +624,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
     const int npair = ncols / 2;
     const size_t stride = static_cast<size_t>(B) * a.per;
     #pragma unroll 1
-    for (int i = tid; i < B * npair; i += nthr) {
+    for (int i = d_thread ? tid : B * npair; i < B * npair; i += nthr_d) {
       const int b = i / npair, lc = 2 * (i - b * npair);
       const float* src = st + static_cast<size_t>(b) * a.per + lc;
       const float x0 = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
@@ -571,25 +633,22 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       dv[0] = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x0), a.at.alpha) : qnan);
       dv[1] = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x1), a.at.alpha) : qnan);
       const uint32_t packed = *reinterpret_cast<const uint32_t*>(dv);
-      const uint32_t slot = smem_addr(sB + b_off(b, c * a.per + lc));  // an even column pair is contiguous
+      const uint32_t slot = smem_addr(sB + b_off(b, rank * a.per + lc));  // an even column pair is contiguous
       for (int pr = 0; pr < C; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
     }
   }
   if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
   #pragma unroll 1
   for (int i = tid; i < B * HS; i += nthr) {
-    const int b = i / HS, h = i - b * HS;
-    float iv = inv_r[0];
-#pragma unroll
-    for (int bb = 1; bb < MB; ++bb)
-      if (bb == b) iv = inv_r[bb];
-    hn_s[i] = norm_hn<T>(hn_s[i], iv, ns_s[h]);
+    const int b = i / HS, m = i - b * HS;
+    hn_s[i] = Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(hn_s[i]), inv_s[b * C + (m >> lgF)], Ty<T>::to_f(ns_s[m])));
   }
   cp_async_wait_all();
   bool dok = true;
   if (split) dok = mbar_wait(dbar, 0, &g_um_wait_timeouts);
   fence_proxy_async_smem();  // A (cp.async) and B (d) visible to the tensor core
   __syncthreads();
+  HC_PHASE(4);
 
   // ---- up^T = Wu^T * d^T: the R16/16 k-steps in NI contiguous ranges, range
   // j issued by lane 0 of warp j into accumulator j (TMEM columns 16j..) ----
@@ -607,9 +666,12 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   }
   const bool mmok = mbar_wait(mma_bar, 0, &g_um_wait_timeouts);
   tc_fence_after();
+  HC_PHASE(5);
 
-  // ---- epilogue: warp w < 4 holds columns 32w..32w+31 (its TMEM lane
-  // quarter), rows in TMEM columns: g = rT(sigmoid(rT(up))), hn*g, pre-mix ----
+  // ---- epilogue: warp w < 4 holds tile columns 32w..32w+31 (its TMEM lane
+  // quarter), rows in TMEM columns: g = rT(sigmoid(rT(up))) and hn*g go to
+  // shared memory; then each feature's C products are summed in branch order
+  // (the pre-mix) and scaled into pre_output ----
   if (warp < 4) {
     // accumulators 0..NI-1 of this lane quarter, added as ((a0 + a1) + (a2 + a3))
     uint32_t acc[kUpIssuers][16];
@@ -628,35 +690,26 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       for (int j = 0; j < kUpIssuers; ++j) x[j] = j < NI ? __uint_as_float(acc[j][r]) : 0.0f;
       v[r] = __fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3]));
     }
-    const int h = warp * 32 + lane;
-    const int j = h / HSc, hl = h - j * HSc;
+    const int m = warp * 32 + lane;
 #pragma unroll
     for (int b = 0; b < MB; ++b)
       if (b < B) {
-        const float up = v[b];
-        const float gg = sigmoid_rT<T>(rT<T>(up));
-        const float prod = (dok && mmok) ? __fmul_rn(hn_s[b * HS + h], gg) : qnan;
-        if (C == 1) {
-          stf(a.pre + static_cast<int64_t>(b) * H + h0 + h, __fmul_rn(a.at.rho, __fadd_rn(0.0f, prod)));
-        } else {
-          st_async_b32(mapa_shared(smem_addr(mix_s + (c * MB + b) * HSc + hl), j), __float_as_uint(prod),
-                       mapa_shared(smem_addr(mbar), j));
-        }
+        const float gg = sigmoid_rT<T>(rT<T>(v[b]));
+        mix_s[b * HS + m] = (dok && mmok) ? __fmul_rn(Ty<T>::to_f(hn_s[b * HS + m]), gg) : qnan;
       }
-  }
-  // ---- pre-mix: rank j sums features [j*HSc, (j+1)*HSc) over c = 0..C-1 ----
-  if (C > 1) {
-    const bool mok = mbar_wait(mbar, 0, &g_um_wait_timeouts);
+    named_bar_sync(1, 128);  // the four epilogue warps
+    HC_PHASE(6);
     #pragma unroll 1
-    for (int i = tid; i < B * HSc; i += nthr) {
-      const int b = i / HSc, hl = i - b * HSc;
+    for (int i = tid; i < B * F; i += 128) {
+      const int b = i / F, f = i - b * F;
       float acc2 = 0.0f;
-      for (int cc = 0; cc < C; ++cc) acc2 = __fadd_rn(acc2, mix_s[(cc * MB + b) * HSc + hl]);
-      stf(a.pre + static_cast<int64_t>(b) * H + h0 + c * HSc + hl, mok ? __fmul_rn(a.at.rho, acc2) : qnan);
+      for (int cb = 0; cb < C; ++cb) acc2 = __fadd_rn(acc2, mix_s[b * HS + cb * F + f]);
+      stf(a.pre + static_cast<int64_t>(b) * H + f0 + f, __fmul_rn(a.at.rho, acc2));
     }
   }
   tc_fence_before();
   __syncthreads();
+  HC_PHASE(7);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 64);
@@ -703,7 +756,7 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.R = R;
   g.down_threads = 12 * 32;  // a multiple of 4 warps (TMEM lane quarters)
   g.KS = 0;
-  for (int ks = 16; ks <= H; ks += 16) {
+  for (int ks = 16; ks <= std::min(H, 256); ks += 16) {  // KS rows: one tensor-copy box (at most 256)
     if (H % ks != 0) continue;
     if (down_smem(8, ks, R, C, cluster_for(H / ks), g.down_threads / 32).total > kUmDownCap) break;
     g.KS = ks;
@@ -715,7 +768,8 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.NCLU = g.NSL / g.CL;
   const Stage sg = stage_for(rows, C, R, g.NCLU, g.NCP);
   if (up_smem(8, R, C, sg.bytes).total > kUmUpCap) return g;
-  g.up_threads = std::min(16, std::max(4, ceil_div(R, 32))) * 32;
+  // warps for the d columns, plus one more: the post gate's (dec_post_gate)
+  g.up_threads = (std::min(15, std::max(4, ceil_div(R, 32))) + 1) * 32;
   g.ok = true;
   return g;
 }
@@ -734,14 +788,41 @@ Layout um_layout(int64_t rows, int C, const UmCfg& g) {
   return L;
 }
 
+// Phase-clock recording (hc_debug_phase_clocks): a caller-owned device buffer
+// of whole slots; each timed call takes the next slot (one per call, so a
+// captured chain of calls keeps every block's record).
+struct PhaseState {
+  unsigned long long* buf = nullptr;
+  size_t slots = 0, next = 0;
+};
+thread_local PhaseState g_phase;
+constexpr size_t kPhaseSlotWords = 2 * kPhaseMaxCtas * kPhasePoints * 2;  // dec_down, then dec_up
+
+template <typename T, int MB, bool TIMED>
+cudaError_t run_um_mb(const Problem& p, const UmCfg& g, unsigned long long* phase);
+
 template <typename T, int MB>
 cudaError_t run_um_mb(const Problem& p, const UmCfg& g) {
+  if constexpr (std::is_same<T, __nv_bfloat16>::value && (MB == 1 || MB == 8)) {
+    if (g_phase.buf != nullptr && g.NSL <= kPhaseMaxCtas && (p.H / kUpHS) * p.C <= kPhaseMaxCtas) {
+      unsigned long long* slot = g_phase.buf + (g_phase.next++ % g_phase.slots) * kPhaseSlotWords;
+      return run_um_mb<T, MB, true>(p, g, slot);
+    }
+  }
+  return run_um_mb<T, MB, false>(p, g, nullptr);
+}
+
+template <typename T, int MB, bool TIMED>
+cudaError_t run_um_mb(const Problem& p, const UmCfg& g, unsigned long long* phase) {
   const Layout WL = um_layout(p.rows, p.C, g);
   char* ws = static_cast<char*>(p.workspace);
   float* inv_ws = reinterpret_cast<float*>(ws + WL.inv);
   float* part_ws = reinterpret_cast<float*>(ws + WL.part);
 
   DownArgs<T> da;
+  if (!make_tmap_2d_sw128(&da.tm_wd, p.down_w, std::is_same<T, __nv_bfloat16>::value, static_cast<uint64_t>(p.R),
+                          static_cast<uint64_t>(p.C) * p.H, static_cast<uint32_t>(g.KS)))
+    return cudaErrorInvalidValue;
   da.streams = static_cast<const T*>(p.streams);
   da.prev_out = static_cast<const T*>(p.prev_out);
   da.prev_gate = static_cast<const T*>(p.prev_gate);
@@ -757,10 +838,16 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g) {
   da.split = sg.split; da.per = sg.per;
   da.eps = p.eps;
   da.weights_static = (p.flags & HC_FLAG_WEIGHTS_STATIC) ? 1 : 0;
+  da.phase = phase;
+  // W_u in NSL equal shares of whole 16-byte units (the tail, if any, is
+  // left to dec_up_um's own copies)
+  da.wu = static_cast<const T*>(p.up_w);
+  da.wu_prefetch_bytes = static_cast<uint32_t>((static_cast<size_t>(p.R) * p.C * p.H * sizeof(T) / g.NSL) & ~size_t{15});
   const size_t dsm = down_smem(MB, g.KS, p.R, p.C, g.CL, g.down_threads / 32).total;
-  cudaError_t e = ensure_smem<dec_down_um<T, MB>>(dsm);
+  cudaError_t e = ensure_smem<dec_down_um<T, MB, TIMED>>(dsm);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(dec_down_um<T, MB>, dim3(g.NSL), dim3(g.down_threads), dsm, p.stream, static_cast<unsigned>(g.CL), da);
+  e = launch_pdl(dec_down_um<T, MB, TIMED>, dim3(g.NSL), dim3(g.down_threads), dsm, p.stream,
+                 static_cast<unsigned>(g.CL), da);
   if (e != cudaSuccess) return e;
 
   UpArgs<T> ua;
@@ -776,11 +863,14 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g) {
   ua.B = da.B; ua.C = p.C; ua.H = p.H; ua.R = p.R; ua.NCLU = g.NCLU; ua.NCP = g.NCP;
   ua.split = sg.split; ua.per = sg.per; ua.st_bytes = sg.bytes;
   ua.at = Attrs{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
+  ua.phase = phase != nullptr ? phase + kPhaseSlotWords / 2 : nullptr;
   const size_t usm = up_smem(MB, p.R, p.C, sg.bytes).total;
-  e = ensure_smem<dec_up_um<T, MB>>(usm);
+  e = ensure_smem<dec_up_um<T, MB, TIMED>>(usm);
   if (e != cudaSuccess) return e;
-  return launch_pdl(dec_up_um<T, MB>, dim3((p.H / kUpHS) * p.C), dim3(g.up_threads), usm, p.stream,
-                    static_cast<unsigned>(p.C), ua);
+  // (H / 128) * C tiles of 128 / C features each; clusters of C CTAs only
+  // where d is split across ranks
+  return launch_pdl(dec_up_um<T, MB, TIMED>, dim3((p.H / kUpHS) * p.C), dim3(g.up_threads), usm, p.stream,
+                    static_cast<unsigned>(sg.split ? p.C : 1), ua);
 }
 
 template <typename T>
@@ -793,8 +883,16 @@ cudaError_t run_um(const Problem& p, const UmCfg& g) {
 
 }  // namespace
 
+size_t set_phase_clocks(void* buf, size_t bytes) {
+  const size_t slot_bytes = kPhaseSlotWords * sizeof(unsigned long long);
+  g_phase.buf = (buf != nullptr && bytes >= slot_bytes) ? static_cast<unsigned long long*>(buf) : nullptr;
+  g_phase.slots = g_phase.buf != nullptr ? bytes / slot_bytes : 0;
+  g_phase.next = 0;
+  return slot_bytes;
+}
+
 bool decode_um_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
-  return um_cfg(rows, C, H, R, dt, 148).ok;
+  return um_cfg(rows, C, H, R, dt, 148).ok && tmap_encoder() != nullptr;
 }
 
 size_t decode_um_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
@@ -806,6 +904,28 @@ cudaError_t launch_decode_um(const Problem& p) {
   const UmCfg g = um_cfg(p.rows, p.C, p.H, p.R, p.dt, p.num_sms);
   if (!g.ok) return cudaErrorInvalidValue;
   return p.dt == HC_F16 ? run_um<__half>(p, g) : run_um<__nv_bfloat16>(p, g);
+}
+
+// One CTA waits, through the same bounded wait as the kernels above, on an
+// mbarrier that nothing arrives on and no copy completes: the wait must give
+// up after `limit` cycles, count itself in the decode kernels' counter, and
+// let the kernel write NaN where its result would go and exit normally.
+__global__ void __launch_bounds__(32) wait_timeout_probe(float* out, long long limit) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  bool ok = true;
+  if (threadIdx.x == 0) ok = mbar_wait_limit(&bar, 0, &g_um_wait_timeouts, limit);
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  out[threadIdx.x] = ok ? 1.0f : __int_as_float(0x7fc00000);
+}
+
+cudaError_t launch_wait_timeout_probe(float* out, long long limit_cycles, cudaStream_t s) {
+  wait_timeout_probe<<<1, 32, 0, s>>>(out, limit_cycles);
+  return cudaGetLastError();
 }
 
 unsigned int read_um_wait_timeouts(bool reset) {

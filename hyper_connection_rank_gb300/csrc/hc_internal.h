@@ -1,6 +1,8 @@
 // Host-side interfaces between the C ABI layer and the kernel launchers.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -50,9 +52,21 @@ bool decode_um_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_um_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode_um(const Problem& p);
 unsigned int read_um_wait_timeouts(bool reset);
+// Phase clocks of the tcgen05 decode pair (bf16, 1 or 8 rows): record into
+// `buf` (slots of the returned size) from the next call on; NULL stops.
+size_t set_phase_clocks(void* buf, size_t bytes);
+// Synchronisation cost probe (hc_sync_probe.cu): mode 0 PDL chain, 1 grid
+// barrier, 2 all-to-all flags; scratch of 32 + ctas words, zeroed by the caller.
+cudaError_t launch_sync_probe(int mode, int ctas, int rounds, size_t smem, unsigned int* scratch, cudaStream_t s);
+// One CTA whose bounded wait on an mbarrier that nothing completes runs out.
+cudaError_t launch_wait_timeout_probe(float* out, long long limit_cycles, cudaStream_t s);
 // Every 16-bit code through the fast rounded sigmoid and the accurate one.
 cudaError_t launch_sigmoid_codes(hc_dtype_t dt, uint16_t* fast, uint16_t* acc, cudaStream_t s);
 cudaError_t launch_sigmoid_table_codes(float* g, cudaStream_t s);
+// The fp16 prefill gate: its table's size, and every fp16 code through it
+// (the table built into `table` first).
+size_t sigmoid_table16_bytes();
+cudaError_t launch_sigmoid_table16_codes(void* table, float* g, cudaStream_t s);
 // Row inverse RMS and Engram gate (hc_rows.cu). `vec`: every pointer 16-byte
 // aligned and the row length a multiple of 16 bytes (16-byte vector loads).
 cudaError_t launch_inv_rms(const void* x, int64_t rows, int64_t dim, float eps, hc_dtype_t dt, float* out, bool vec,
@@ -74,6 +88,15 @@ bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t prefill_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 cudaError_t launch_prefill(const Problem& p);
 unsigned int read_pf_wait_timeouts(bool reset);
+
+// Tensor (TMA) maps (hc_tmap.cu): the driver's encoder (nullptr if the
+// driver lacks it), and a map over a row-major [outer, inner] matrix of 16-bit
+// elements (inner * 2 bytes a multiple of 16, base 16-byte aligned), box {64,
+// box_outer}, 128-byte swizzle: each box lands as box_outer rows of 128 bytes,
+// 16-byte chunk j of row r at chunk j ^ (r % 8); columns past `inner` read 0.
+PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder();
+bool make_tmap_2d_sw128(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer,
+                        uint32_t box_outer);
 
 // Record `msg` as this thread's hc_last_error() text and return `s`.
 hc_status_t set_error(hc_status_t s, const char* msg);

@@ -24,10 +24,8 @@
 // Pipelines: one TMA thread, one MMA thread, four epilogue warps; stage
 // hand-off through mbarriers (all waits bounded, see hc_async.cuh).
 #include <cuda.h>
-#include <cudaTypedefs.h>
 
 #include <algorithm>
-#include <mutex>
 
 #include "hc_async.cuh"
 #include "hc_common.cuh"
@@ -181,6 +179,7 @@ struct PfUpArgs {
   CUtensorMap tm_b;  // up_w  [R, C*H],    box {64 n, 64 k}
   CUtensorMap tm_hn; // hn tiles [row tiles * C*H/64][128][64], box {64 features, 128 rows, 1}
   const T* hn;       // tiled, as tm_hn
+  const uint16_t* sig16;  // fp16: the gate table built by pf_sig16_table (kS16Bytes)
   T* pre;            // [rows, H]
   int rows, C, H, R, stages, nbuf;
   float rho;
@@ -475,10 +474,11 @@ __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __res
 // NaN); a sign bit moved to bit 11 selects the negative half of the table. The
 // table holds bf16 values and hn * g + acc is one mixed-precision fused
 // multiply-add (bf16 operands, fp32 addend): no operand is widened first. fp16
-// (whose non-constant range is too wide for a table in shared memory) uses
-// sigmoid_rT, the fast sigmoid that falls back to the accurate form near a
-// rounding midpoint of T: the same bits as the accurate rounded sigmoid on
-// every fp16 input.
+// does the same with its own table (kS16*, below), which is too large to
+// rebuild in every CTA: pf_sig16_table builds it once per call and each CTA
+// copies it in (and runs two operand stages instead of three to make room).
+// The exact fast sigmoid on the arithmetic pipes was measured slower in both
+// types: it needs two MUFU operations per element.
 constexpr int kUpEpiWarps = 16;
 constexpr int kUpHnWarp = 2 + kUpEpiWarps;                 // the warp that loads hn
 constexpr int kUpThreads = 32 * (kUpHnWarp + 1);
@@ -493,8 +493,22 @@ constexpr int kSigHalf = 2048;              // entries per sign; a power of two 
 constexpr int kSigBytes = 2 * kSigHalf * 2; // bf16 entries
 static_assert(static_cast<int>(kSigNaN - kSigLo) < kSigHalf, "sigmoid table half too small");
 
+// fp16: the same lookup over fp16 codes. g = rT(sigmoid(u)) is 1/2 below
+// 2^-12 (|u|/4 stays under half an ulp of 1/2), 1 from u = 9 on and 0 from
+// u = -18 down; the table spans the magnitude codes between (one half per
+// sign, 16516 entries each: not a power of two, so the sign selects its half
+// by a multiply). Too large to rebuild in every CTA, it is built once per call
+// by pf_sig16_table into the workspace and copied into each pf_up CTA.
+constexpr uint32_t kS16Lo = 0x0BFFu;          // largest fp16 magnitude code below 2^-12
+constexpr uint32_t kS16PosHi = 0x4880u;       // 9.0
+constexpr uint32_t kS16NegHi = 0x4C80u;       // 18.0
+constexpr uint32_t kS16NaN = kS16NegHi + 1;   // the magnitude code NaN is moved to
+constexpr int kS16Half = 16516;               // >= kS16NaN - kS16Lo + 1, even
+constexpr int kS16Bytes = 2 * kS16Half * 2;
+static_assert(static_cast<int>(kS16NaN - kS16Lo) < kS16Half, "fp16 sigmoid table half too small");
+
 struct UpBars {
-  uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[kHnSlotsMax], hne[kHnSlotsMax];
+  uint64_t full[kUpStages], empty[kUpStages], accf[2], acce[2], hnf[kHnSlotsMax], hne[kHnSlotsMax], tab;
   uint32_t tmem_base;
 };
 
@@ -536,6 +550,65 @@ __device__ __forceinline__ void sig_pair_fma(const uint16_t* tab, uint32_t hn2, 
       : "r"(hn2), "h"(g0), "h"(g1));
 }
 
+// Entry i of the fp16 table: sign i / kS16Half, magnitude code kS16Lo + i % kS16Half.
+__device__ __forceinline__ uint16_t sig16_entry(int i) {
+  const uint32_t neg = static_cast<uint32_t>(i) >= static_cast<uint32_t>(kS16Half) ? 1u : 0u;
+  const uint32_t m = kS16Lo + static_cast<uint32_t>(i) - neg * kS16Half;
+  if (m == kS16NaN) return 0x7E00u;                       // NaN
+  if (m > (neg ? kS16NegHi : kS16PosHi)) return 0;        // never read
+  const float u = __half2float(__ushort_as_half(static_cast<uint16_t>((neg << 15) | m)));
+  return __half_as_ushort(__float2half_rn(sigmoid_acc(u)));
+}
+
+// The fp16 table, one entry per thread (grid-stride). Launched between
+// pf_norm and pf_down when chained: it lets pf_down launch at once and, before
+// it ends, waits for pf_norm, so that pf_down's dependency wait still covers
+// pf_norm (programmatic dependence reaches only the previous kernel).
+__global__ void __launch_bounds__(256) pf_sig16_table(uint16_t* tab, int chained) {
+  pdl_trigger();
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < 2 * kS16Half; i += gridDim.x * blockDim.x)
+    tab[i] = sig16_entry(i);
+  if (chained) pdl_wait();
+}
+
+// acc0 += hn0 * g(up0), acc1 += hn1 * g(up1) for a pair of fp16 hn values,
+// g from the fp16 table (as sig_pair_fma does for bf16).
+__device__ __forceinline__ void sig16_pair_fma(const uint16_t* tab, uint32_t hn2, float up0, float up1, float& acc0,
+                                               float& acc1) {
+  uint32_t v2, m2;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(v2) : "f"(up1), "f"(up0));
+  asm("max.NaN.f16x2 %0, %0, %1;" : "+r"(v2) : "r"(0xCC80CC80u));  // -18
+  asm("min.NaN.f16x2 %0, %0, %1;" : "+r"(v2) : "r"(0x48804880u));  // 9
+  m2 = v2 & 0x7FFF7FFFu;
+  asm("max.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(kS16Lo * 0x10001u));
+  asm("min.u16x2 %0, %0, %1;" : "+r"(m2) : "r"(kS16NaN * 0x10001u));
+  const uint32_t idx2 = m2 + ((v2 >> 15) & 0x00010001u) * static_cast<uint32_t>(kS16Half) - kS16Lo * 0x10001u;
+  const uint16_t g0 = tab[idx2 & 0xFFFFu], g1 = tab[idx2 >> 16];
+  asm("{\n\t.reg .b16 h0, h1;\n\t"
+      "mov.b32 {h0, h1}, %2;\n\t"
+      "fma.rn.f32.f16 %0, h0, %3, %0;\n\t"
+      "fma.rn.f32.f16 %1, h1, %4, %1;\n\t}"
+      : "+f"(acc0), "+f"(acc1)
+      : "r"(hn2), "h"(g0), "h"(g1));
+}
+
+// The fp16 epilogue's gate for every fp16 code (diagnostic for
+// hc_debug_sigmoid_table_f16), from a table built by pf_sig16_table: one pair
+// of codes per thread, hn = 1, zero sums.
+__global__ void __launch_bounds__(256) sigmoid_table16_codes(const uint16_t* table, float* g) {
+  extern __shared__ uint16_t tab16[];
+  for (int i = threadIdx.x; i < 2 * kS16Half; i += blockDim.x) tab16[i] = table[i];
+  __syncthreads();
+  const int p = blockIdx.x * blockDim.x + threadIdx.x;  // codes 2p, 2p + 1
+  if (p >= 32768) return;
+  const float u0 = __half2float(__ushort_as_half(static_cast<uint16_t>(2 * p)));
+  const float u1 = __half2float(__ushort_as_half(static_cast<uint16_t>(2 * p + 1)));
+  float a0 = 0.0f, a1 = 0.0f;
+  sig16_pair_fma(tab16, 0x3C003C00u, u0, u1, a0, a1);  // hn = (1, 1)
+  g[2 * p] = a0;
+  g[2 * p + 1] = a1;
+}
+
 // The epilogue's gate for every bf16 code (diagnostic for
 // hc_debug_sigmoid_table): one pair of codes per thread, hn = 1, zero sums.
 __global__ void __launch_bounds__(256) sigmoid_table_codes(float* g) {
@@ -559,12 +632,12 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = a.C, H = a.H, R = a.R, NH = a.nbuf;
   const int G = (C + 3) / 4, GC = C < 4 ? C : 4;        // groups per tile, branches per group
-  const int nk = R / kBK, NG = 64 * GC;
+  const int nk = R / kBK, NG = 64 * GC, S = a.stages;  // S operand stages, at most 3
   const int stage_bytes = kATileBytes + GC * kBoxBytes;  // d box, then W_u of one K block for the group
-  uint8_t* st_s = smem;                                  // [kUpStages][d box | GC][...]
-  uint8_t* hn_s = st_s + kUpStages * stage_bytes;        // [NH][128 rows][64] (swizzled)
+  uint8_t* st_s = smem;                                  // [S][d box | GC][...]
+  uint8_t* hn_s = st_s + S * stage_bytes;                // [NH][128 rows][64] (swizzled)
   uint16_t* sig = reinterpret_cast<uint16_t*>(hn_s + NH * kHnBoxBytes);
-  UpBars* pb = reinterpret_cast<UpBars*>(reinterpret_cast<uint8_t*>(sig) + kSigBytes);
+  UpBars* pb = reinterpret_cast<UpBars*>(reinterpret_cast<uint8_t*>(sig) + (BF16 ? kSigBytes : kS16Bytes));
   const int n_h = H / 64, n_m = (a.rows + kBM - 1) / kBM, n_tiles = n_m * n_h;
   const uint32_t ncols = tmem_cols_for(2 * NG);
 
@@ -572,7 +645,15 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     for (int i = threadIdx.x; i < 2 * kSigHalf; i += blockDim.x) sig[i] = sig_entry(i);
   }
   if (warp == 0 && lane == 0) {
-    for (int st = 0; st < kUpStages; ++st) {
+    if (!BF16) {
+      // the fp16 table, written by pf_sig16_table three kernels back (pf_up
+      // starts only after pf_mid's dependency wait): copied before ours
+      mbar_init(&pb->tab, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&pb->tab, static_cast<uint32_t>(kS16Bytes));
+      bulk_g2s(sig, a.sig16, static_cast<uint32_t>(kS16Bytes), &pb->tab);
+    }
+    for (int st = 0; st < S; ++st) {
       mbar_init(&pb->full[st], 1);
       mbar_init(&pb->empty[st], 1);
     }
@@ -609,8 +690,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
         for (int g = 0; g < G && ok; ++g) {
           const int c_lo = g * 4, nc = min(4, C - c_lo);
           for (int kb = 0; kb < nk; ++kb, ++it) {
-            const int st = it % kUpStages;
-            ok = mbar_wait(&pb->empty[st], ((it / kUpStages) & 1) ^ 1, &g_pf_wait_timeouts);
+            const int st = it % S;
+            ok = mbar_wait(&pb->empty[st], ((it / S) & 1) ^ 1, &g_pf_wait_timeouts);
             if (!ok) break;
             uint8_t* sp = st_s + st * stage_bytes;
             mbar_arrive_expect_tx(&pb->full[st], static_cast<uint32_t>(kATileBytes + nc * kBoxBytes));
@@ -655,8 +736,8 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
           const uint32_t dbase = tmem + static_cast<uint32_t>(buf * NG);
           const uint32_t idn = idesc_f16(BF16, kBM, 64 * nc, false, true);
           for (int kb = 0; kb < nk; ++kb, ++it) {
-            const int st = it % kUpStages;
-            ok = mbar_wait(&pb->full[st], (it / kUpStages) & 1, &g_pf_wait_timeouts);
+            const int st = it % S;
+            ok = mbar_wait(&pb->full[st], (it / S) & 1, &g_pf_wait_timeouts);
             if (!ok) break;
             tc_fence_after();
             // descriptors stepped by constants, as in pf_down
@@ -679,7 +760,7 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
     const int ew = warp - 2, lq = warp & 3, hc = ew >> 2;
     const int row = lq * 32 + lane;
     int unit = 0, hseq = 0;
-    bool ok = true;
+    bool ok = true, tab_ready = false;
     for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
       const int m0 = (tile / n_h) * kBM, h0 = (tile % n_h) * 64;
       const int64_t grow = m0 + row;
@@ -713,17 +794,15 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
               sig_pair_fma(sig, hw[i], __uint_as_float(up[2 * i]), __uint_as_float(up[2 * i + 1]), acc[2 * i],
                            acc[2 * i + 1]);
           } else {
-            float hf[16];
-            V8<T>::unpack(v0, hf);
-            V8<T>::unpack(v1, hf + 8);
-            // g = rT(sigmoid(u)) bit for bit as the accurate form rounds it
-            // (sigmoid_rT: fast evaluation, the accurate one near a rounding
-            // midpoint of T); hn * g is exact in fp32 (two 16-bit
-            // significands), so the fused multiply-add gives the bits of the
-            // separate multiply and add
+            if (!tab_ready) {
+              ok = mbar_wait(&pb->tab, 0, &g_pf_wait_timeouts) && ok;
+              tab_ready = true;
+            }
+            const uint32_t hw[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[j] = fmaf(hf[j], sigmoid_rT<T>(rT<T>(__uint_as_float(up[j]))), acc[j]);
+            for (int i = 0; i < 8; ++i)
+              sig16_pair_fma(sig, hw[i], __uint_as_float(up[2 * i]), __uint_as_float(up[2 * i + 1]), acc[2 * i],
+                             acc[2 * i + 1]);
           }
           // the slot is released only after every lane has used what it read
           // from it, and each lane first orders its (generic-proxy) reads
@@ -758,37 +837,14 @@ __global__ void __launch_bounds__(kUpThreads, 1) pf_up(const __grid_constant__ P
 
 // ------------------------------------------------------------------ host --
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static std::once_flag once;
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  std::call_once(once, []() {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2D tiled map over a row-major [outer, inner] tensor of 16-bit elements,
-// box {64, box_outer}, 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer, uint32_t box_outer) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner * 2};
-  const cuuint32_t box[2] = {64, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base),
-            dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return make_tmap_2d_sw128(m, base, bf16, inner, outer, box_outer);
 }
 
 // 3D map over 16-bit tiles of 128 rows x 64 columns stored contiguously
 // ([tile][row][column]), box = one whole tile, 128-byte swizzle.
 bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, uint64_t tiles) {
-  auto fn = encode_fn();
+  auto fn = tmap_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(kBM), tiles};
   const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(kBM) * 128};
@@ -804,7 +860,7 @@ bool make_tile_map(CUtensorMap* m, const void* base, bool bf16, uint64_t tiles) 
 // `box_rows` rows, 128-byte swizzle. One copy then lands the chunks one after
 // another in shared memory, each a 128-byte-swizzled MN-major block.
 bool make_chunk_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner, uint64_t outer, uint32_t box_rows) {
-  auto fn = encode_fn();
+  auto fn = tmap_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {64, outer, inner / 64};
   const cuuint64_t strides[2] = {inner * 2, 128};
@@ -820,7 +876,7 @@ bool make_chunk_map(CUtensorMap* m, const void* base, bool bf16, uint64_t inner,
 // copy lands a K block of 64 columns of gc consecutive branches, branch after
 // branch, each a 128-byte-swizzled MN-major block.
 bool make_branch_map(CUtensorMap* m, const void* base, bool bf16, uint64_t H, uint64_t R, uint64_t C, uint32_t gc) {
-  auto fn = encode_fn();
+  auto fn = tmap_encoder();
   if (fn == nullptr) return false;
   const cuuint64_t dims[3] = {H, R, C};
   const cuuint64_t strides[2] = {C * H * 2, H * 2};
@@ -849,7 +905,7 @@ int k_per_split_for(int64_t rows, int C, int H) {
 }
 
 struct PfLayout {
-  size_t hn, part, d, total;
+  size_t hn, part, d, sig16, total;
 };
 PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   const size_t es = dtype_size(dt), CH = static_cast<size_t>(C) * H;
@@ -858,7 +914,8 @@ PfLayout pf_layout(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   L.hn = 0;  // whole 128-row tiles
   L.part = align_up(L.hn + static_cast<size_t>((rows + kBM - 1) / kBM) * kBM * CH * es, 256);
   L.d = align_up(L.part + ksplit * rows * (R + 16) * 4, 256);
-  L.total = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);
+  L.sig16 = align_up(L.d + rows * static_cast<size_t>(R) * es, 256);  // fp16: the gate table
+  L.total = align_up(L.sig16 + (dt == HC_F16 ? static_cast<size_t>(kS16Bytes) : 0), 256);
   return L;
 }
 
@@ -889,6 +946,12 @@ cudaError_t run_prefill(const Problem& p) {
     default: e = ensure_smem<pf_norm<T, 8>>(nsm); if (e == cudaSuccess) e = norm(pf_norm<T, 8>); break;
   }
   if (e != cudaSuccess) return e;
+  uint16_t* sig16 = reinterpret_cast<uint16_t*>(ws + WL.sig16);
+  if (!BF16) {
+    // the fp16 gate table, between pf_norm and pf_down (see pf_sig16_table)
+    e = launch_pdl(pf_sig16_table, dim3((2 * kS16Half + 255) / 256), dim3(256), 0, p.stream, 1u, sig16, 1);
+    if (e != cudaSuccess) return e;
+  }
 
   const unsigned mtiles = static_cast<unsigned>((rows + kBM - 1) / kBM);
   PfDownArgs da;
@@ -925,15 +988,17 @@ cudaError_t run_prefill(const Problem& p) {
       !make_tile_map(&ua.tm_hn, hn, BF16, hn_tiles))
     return cudaErrorInvalidValue;
   ua.hn = hn;
+  ua.sig16 = sig16;
   ua.pre = static_cast<T*>(p.pre_output);
   ua.rows = static_cast<int>(rows);
   ua.C = C; ua.H = H; ua.R = R;
   ua.rho = p.rho;
-  ua.stages = kUpStages;
-  // shared memory: the operand stages, the sigmoid table and barriers, then
-  // as many hn slots (2..6) as the budget leaves
-  const size_t fixed = 1024 + static_cast<size_t>(kUpStages) * (kATileBytes + GC * kBoxBytes) + kSigBytes +
-                       sizeof(UpBars);
+  // shared memory: the operand stages (two in fp16, whose table is larger),
+  // the sigmoid table and barriers, then as many hn slots (2..6) as the
+  // budget leaves
+  ua.stages = BF16 ? kUpStages : 2;
+  const size_t fixed = 1024 + static_cast<size_t>(ua.stages) * (kATileBytes + GC * kBoxBytes) +
+                       (BF16 ? kSigBytes : kS16Bytes) + sizeof(UpBars);
   const int nh = static_cast<int>(std::min<size_t>(kHnSlotsMax, (kSmemBudget - fixed) / kHnBoxBytes));
   if (nh < 2) return cudaErrorInvalidValue;
   ua.nbuf = nh;
@@ -952,13 +1017,24 @@ cudaError_t launch_sigmoid_table_codes(float* g, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+size_t sigmoid_table16_bytes() { return kS16Bytes; }
+
+cudaError_t launch_sigmoid_table16_codes(void* table, float* g, cudaStream_t s) {
+  pf_sig16_table<<<(2 * kS16Half + 255) / 256, 256, 0, s>>>(static_cast<uint16_t*>(table), 0);
+  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = ensure_smem<sigmoid_table16_codes>(kS16Bytes);
+  if (e != cudaSuccess) return e;
+  sigmoid_table16_codes<<<128, 256, kS16Bytes, s>>>(static_cast<const uint16_t*>(table), g);
+  return cudaGetLastError();
+}
+
 bool prefill_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt) {
   if (dt != HC_BF16 && dt != HC_F16) return false;
   if (rows < 9 || rows > (int64_t{1} << 24)) return false;
   if (!(C == 1 || C == 2 || C == 4 || C == 8)) return false;
   if (H % 64 != 0 || R % 64 != 0 || R > 448) return false;  // R + 16 inject columns <= 512
   if (static_cast<int64_t>(C) * H > kNormVec * kNormMaxThreads * 8) return false;
-  return encode_fn() != nullptr;
+  return tmap_encoder() != nullptr;
 }
 
 size_t prefill_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt) {

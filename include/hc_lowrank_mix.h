@@ -160,6 +160,62 @@ const char* hc_last_error(void);
  * Synchronises with the current device; reset != 0 clears the count. */
 unsigned int hc_debug_wait_timeouts(int reset);
 
+/* Diagnostic, with no counterpart on the page that defines the block (it
+ * backs the choice of two kernels per decode block over one; the page's
+ * research one-kernel variant, "Benchmark", used a grid barrier): enqueues
+ * `rounds` repetitions of one synchronisation mechanism over `ctas` CTAs of
+ * 128 threads that each reserve smem_bytes of shared memory, for the caller
+ * to time with events around the call:
+ *   mode 0: a chain of `rounds` kernels linked by programmatic dependent
+ *           launch, as between the decode pair's two kernels;
+ *   mode 1: one cooperative kernel crossing `rounds` grid barriers (one
+ *           counter, release add and acquire poll);
+ *   mode 2: one cooperative kernel in which, per round, every CTA publishes
+ *           a flag and polls every other CTA's flag.
+ * scratch: device buffer owned by the caller, at least (32 + ctas) 32-bit
+ * words, 16-byte aligned, ZEROED by the caller before each call; word 0
+ * counts polls that gave up (every poll is bounded, about 0.1 s in all, so
+ * the kernel always ends; 0 in a valid run). Limits: ctas 1..1024, rounds
+ * 1..100000, smem_bytes <= 200 KB. Modes 1 and 2 fail with HC_ERR_CUDA
+ * (cooperative launch too large) rather than start when the CTAs cannot all
+ * be resident at once. */
+hc_status_t hc_debug_sync_probe(int mode, int ctas, int rounds, size_t smem_bytes, void* scratch,
+                                size_t scratch_bytes, struct CUstream_st* stream);
+
+/* Diagnostic, with no counterpart on the page that defines the block: phase
+ * clocks of the decode path's two tensor-core kernels, to attribute the time
+ * of a block to its steps. From the next hc_lowrank_mix call on the calling
+ * thread that runs them in bf16 with 1 or 8 rows, each such call writes one
+ * slot of `buf` (device memory owned by the caller; consecutive calls take
+ * consecutive slots, wrapping after bytes / slot size of them, so every call
+ * of a captured chain keeps its own). A slot holds, for the down kernel and
+ * then the up kernel, 256 CTAs x 10 points x {globaltimer ns, SM clock64}
+ * (unsigned 64-bit), written by thread 0 of each CTA at the points:
+ *   down: 0 entry, 1 weights issued, 2 dependency wait returned, 3 S pass
+ *         done, 4 inverse RMS ready, 5 weights landed, 6 MMA operands ready,
+ *         7 MMA done, 8 cluster exchange landed, 9 partial sums written;
+ *   up:   0 entry, 1 prefetches issued, 2 dependency wait returned, 3 partial
+ *         sums landed, 4 MMA operands ready, 5 MMA done, 6 pre-mix products
+ *         landed, 7 pre_output written.
+ * Entries of CTAs beyond the grid and of unused points are left untouched.
+ * buf == NULL (or bytes below one slot) stops the recording. Returns the slot
+ * size in bytes. The timed kernels compute the same results; they are slower
+ * only by the stamps. */
+size_t hc_debug_phase_clocks(void* buf, size_t bytes);
+
+/* Diagnostic, with no counterpart on the page that defines the block: makes
+ * one bounded device wait run out on purpose, so that the give-up path can be
+ * checked without faulting or hanging the GPU. One CTA of 32 threads waits,
+ * through the same bounded mbarrier wait the kernels use, on an mbarrier that
+ * nothing arrives on and no copy completes, for at most limit_cycles SM clock
+ * cycles (1e3 .. 4e9; about 2e6 per millisecond); the wait then gives up,
+ * adds one to the count hc_debug_wait_timeouts reports, and the kernel writes
+ * NaN to out[0..31] (1.0f where the wait had succeeded) and exits normally.
+ * out: device buffer of 32 floats, owned by the caller. Asynchronous on
+ * `stream`. HC_ERR_INVALID_ARG for a null pointer or a limit outside the
+ * range, HC_ERR_CUDA if the launch fails. */
+hc_status_t hc_debug_wait_timeout(float* out, long long limit_cycles, struct CUstream_st* stream);
+
 /* Diagnostic, with no counterpart on the page that defines the block: check of
  * the fast sigmoid the fp16/bf16 kernels use where the contract rounds
  * sigmoid(z) to T for a z that is itself a value of T (the ScaledSiLU gate and
@@ -183,6 +239,21 @@ hc_status_t hc_debug_sigmoid_exact(hc_dtype_t dtype, void* fast_out, void* acc_o
  * Asynchronous on `stream`. HC_ERR_INVALID_ARG for a null pointer,
  * HC_ERR_CUDA if the launch fails. */
 hc_status_t hc_debug_sigmoid_table(float* g_out, struct CUstream_st* stream);
+
+/* Diagnostic, with no counterpart on the page that defines the block: the
+ * same check for the fp16 prefill epilogue, whose gate table is built per call
+ * by a kernel of its own (into the workspace) and copied into each CTA. The
+ * table is built into `table` (device scratch owned by the caller, at least
+ * hc_debug_sigmoid_table_f16_bytes() bytes, 16-byte aligned), then the gate
+ * is formed from it as the epilogue forms it (packed clamps, lookup, the
+ * mixed-precision multiply-add of hn * g with hn = 1 and a zero sum) for the up
+ * value of each of the 65536 fp16 codes x: g_out[x] (fp32, 65536 floats,
+ * caller-owned) must equal the accurate rounded sigmoid of x for every code
+ * (NaN for NaN). Asynchronous on `stream`. HC_ERR_INVALID_ARG for a null
+ * pointer, HC_ERR_WORKSPACE for a short or misaligned table buffer,
+ * HC_ERR_CUDA if a launch fails. */
+size_t hc_debug_sigmoid_table_f16_bytes(void);
+hc_status_t hc_debug_sigmoid_table_f16(float* g_out, void* table, size_t table_bytes, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }
