@@ -6,21 +6,30 @@ make a per-element bound on pre_output ill-posed, and elements that miss the
 plain bound are re-judged for them, each count reported:
   1. cancellation: pre_output is a signed sum over the branches, so the bound
      is applied at the condition-aware magnitude max(|pre|, |rho| sum_c |hn g|);
-  2. intermediate rounding flips: the contract rounds down, d, up, hn and g
-     to T; any accumulation order other than the oracle's sequential one (the
-     tensor cores' fp32 accumulation in particular) moves some fp32 values
-     across a rounding boundary of T, flipping them by one ulp, and a flip
-     propagates. The element then passes if it is within 2 ulp of the
-     condition-aware magnitude plus the first-order effect of a one-ulp flip
-     at every rounding site feeding it, propagated with the oracle's values:
+  2. intermediate rounding flips: the contract ("Numerics contract") fixes
+     where values are rounded to T (down, d, up, hn, g among them) but not the
+     order of the fp32 sums before them; any order other than the oracle's
+     sequential one (the tensor cores' fp32 accumulation in particular) moves
+     an fp32 value that lies next to a rounding midpoint of T to the other
+     side, so the rounded value differs by one ulp, and the flip propagates.
+     At C = 1 nothing cancels it: a flip of up flips g, and rho * hn * g moves
+     by up to 2 ulp more (seen: 3 and 4 ulp). The element then passes if it is
+     within 2 ulp of the condition-aware magnitude plus the first-order effect
+     of ONE flip at each rounding site of its own chain (its up and g, its
+     branches' hn) and of one flip among the d values feeding it, propagated
+     with the oracle's values:
        dd   = 2 ulp(d) + (SG + |alpha down| SG (1 - SG)) ulp(down)
-       dup  = ulp(up) + dd @ |W_u|
+       dup  = ulp(up) + max_r dd_r * max_r |W_u[r, n]|
        dg   = ulp(g) + g (1 - g) dup
        dpre = |rho| sum_c (|hn| dg + ulp(hn) |g|).
-A flip-driven drift must stay rare: for float16 / bfloat16 at least 85% of
-pre_output elements must be bit-identical to the oracle (a missing rounding
-site or a wrong order shows up as a far lower figure). streams_out must match
-bit for bit.
+     Such elements must stay rare and close: at most FLIP_CAP_FRAC of a call's
+     elements (at least FLIP_CAP_MIN) and each within FLIP_CAP_ULP ulp; more
+     means something other than isolated flips (a wrong site or order).
+Every element outside the plain bound is counted per tier with its largest
+ulp distance (``compare`` returns them and appends them to HC_PARITY_LOG). For
+float16 / bfloat16 at least 85% of pre_output elements must be bit-identical
+to the oracle (a missing rounding site or a wrong order shows up as a far lower
+figure). streams_out must match bit for bit.
 """
 from __future__ import annotations
 
@@ -34,6 +43,7 @@ import oracle
 from _util import DT_CODE, codes_to_f64, to_codes, ulp_diff
 
 KEYS = ("streams", "norm_scale", "down_w", "up_w", "inject_w", "prev_out", "prev_gate")
+FLIP_CAP_FRAC, FLIP_CAP_MIN, FLIP_CAP_ULP = 1e-4, 2, 6
 SIG_BITS = {"f32": 24, "f16": 11, "bf16": 8}
 DT_OF = {torch.float32: "f32", torch.float16: "f16", torch.bfloat16: "bf16"}
 
@@ -65,14 +75,15 @@ def run_gpu(hc, d, C, attrs, flags=0, want_streams_out=True, device="cuda"):
 
 
 def flip_bound(t, inputs, dt, rows, C, H, R, attrs):
-    """First-order bound on |pre - oracle pre| from one-ulp flips at the
-    contract's rounding sites (see the module docstring)."""
+    """First-order bound on |pre - oracle pre| from single one-ulp flips at
+    the contract's rounding sites along each element's chain (see the module
+    docstring)."""
     u = lambda x: spacing(x, dt)
     down, sg, d = (t[k].astype(np.float64) for k in ("down", "SG", "hidden"))
     up, g, hn = (t[k].astype(np.float64) for k in ("up", "g", "hn"))
     dd = 2 * u(d) + (np.abs(sg) + np.abs(attrs["silu_alpha"] * down) * sg * (1 - sg)) * u(down)
-    wu = np.abs(inputs["up_w"].to(torch.float64).numpy())
-    dup = u(up) + dd @ wu
+    wu_max = np.abs(inputs["up_w"].to(torch.float64).numpy()).max(0)
+    dup = u(up) + dd.max(1, keepdims=True) * wu_max[None, :]
     dg = u(g) + g * (1 - g) * dup
     hn3, g3, dg3 = hn.reshape(rows, C, H), g.reshape(rows, C, H), dg.reshape(rows, C, H)
     return abs(attrs["reduction_scale"]) * (np.abs(hn3) * dg3 + u(hn3) * np.abs(g3)).sum(1)
@@ -125,6 +136,10 @@ def compare(gpu, ref, dt, C, H, R, attrs, check_streams_out=True, inputs=None):
     stats["post_max_ulp"] = int(ulp_diff(gpost, opost, dt)[finq].max()) if finq.any() else 0
     stats["fail"] = int((~ok).sum())
     log_stats(stats, dt)
+    cap = max(FLIP_CAP_MIN, int(FLIP_CAP_FRAC * gpre.size))
+    assert stats["pre_flip_rescued"] <= cap, (f"{stats['pre_flip_rescued']} elements need the rounding-flip tier "
+                                              f"(cap {cap})")
+    assert stats["pre_flip_max_ulp"] <= FLIP_CAP_ULP, f"a flip-tier element is {stats['pre_flip_max_ulp']} ulp off"
     if dt != "f32" and gpre.size >= 1000:
         assert stats["pre_bit_identical"] >= 0.85, f"only {stats['pre_bit_identical']:.3f} of pre_output bit-identical"
     bad = np.argwhere(~ok)

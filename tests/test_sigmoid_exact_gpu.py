@@ -77,3 +77,23 @@ def test_prefill_table_gate_equals_accurate_on_every_code(hc):
     assert not low.any(), "gate is not a bf16 value"
     bad = np.nonzero(gb != a[~nan_in])[0]
     assert bad.size == 0, f"{bad.size} codes differ, e.g. {np.arange(65536)[~nan_in][bad[:8]].tolist()}"
+
+
+def test_prefill_fp16_table_gate_equals_accurate_on_every_code(hc):
+    """The fp16 prefill epilogue's gate (the table built per call, packed
+    clamps, mixed-precision multiply-add) on every fp16 code of up against
+    the accurate rounded sigmoid evaluated by the library, code for code;
+    NaN gives NaN."""
+    g = hc.debug_sigmoid_table_f16()
+    _, acc = hc.debug_sigmoid_exact(torch.float16)
+    torch.cuda.synchronize()
+    g = g.cpu().numpy()
+    a = acc.cpu().numpy().view(np.uint16)
+    xs = oracle.to_float(np.arange(65536, dtype=np.uint16), 1)
+    nan_in = np.isnan(xs)
+    assert np.isnan(g[nan_in]).all()
+    # g is an fp16 value carried in fp32: converting it to fp16 is exact
+    gh = g[~nan_in].astype(np.float16)
+    assert np.array_equal(gh.astype(np.float32), g[~nan_in]), "gate is not an fp16 value"
+    bad = np.nonzero(gh.view(np.uint16) != a[~nan_in])[0]
+    assert bad.size == 0, f"{bad.size} codes differ, e.g. {np.arange(65536)[~nan_in][bad[:8]].tolist()}"
