@@ -169,6 +169,10 @@ def run_ours(args, rank, world, local_rank):
     rows = args.rows
     flags = hc.HC_FLAG_WEIGHTS_STATIC
     assert hc.path(rows, C, H, R, torch.bfloat16, flags) == hc.HC_PATH_DECODE
+    if args.profile_case == "phases":
+        return profile_phases(args, hc, I, dev, rows, flags)
+    if args.profile_case == "sync":
+        return {"profile_case": "synchronisation cost probe", "sync_costs": sync_costs(hc, dev)}
     if args.profile_case:
         return profile_case(args, hc, I, dev, rows, flags)
     weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(NSETS)]
@@ -256,8 +260,72 @@ def run_ours(args, rank, world, local_rank):
         del weights
         torch.cuda.empty_cache()
         result["isolated"] = isolated_latency(hc, I, dev, pk)
+        result["sync_costs"] = sync_costs(hc, dev)
         result["sweep"] = sweep(hc, I, dev, pk)
     return result
+
+
+def sync_costs(hc, dev, ctas=128, smem=100 * 1024, rounds=(500, 1000)):
+    """What one all-to-all synchronisation of 128 CTAs costs (hc_debug_sync_probe),
+    per round, as the slope between two round counts (so launch costs drop
+    out): a kernel boundary with programmatic dependent launch (the chain of
+    kernels captured in a CUDA graph, as the decode pair runs), a software
+    grid barrier and an all-to-all flag exchange (one cooperative kernel
+    each). Each CTA reserves 100 KB of shared memory, like a decode CTA (two
+    fit on an SM, as the decode pair's two kernels do)."""
+    import torch
+    from hyper_connection_rank_gb300 import _binding as B
+    L = B.lib()
+    scratch = torch.zeros(32 + ctas, dtype=torch.int32, device=dev)
+    nbytes = scratch.numel() * 4
+
+    def call(mode, r, stream):
+        st = L.hc_debug_sync_probe(mode, ctas, r, smem, scratch.data_ptr(), nbytes, stream.cuda_stream)
+        if st != 0:
+            B.check(st)
+
+    out = {}
+    for mode, name in ((0, "pdl_kernel_boundary"), (1, "grid_barrier"), (2, "flag_all_to_all")):
+        t = {}
+        for r in rounds:
+            scratch.zero_()
+            cur = torch.cuda.current_stream(dev)
+            call(mode, 4, cur)
+            torch.cuda.synchronize()
+            if mode == 0:
+                g = torch.cuda.CUDAGraph()
+                side = torch.cuda.Stream(dev)
+                side.wait_stream(cur)
+                with torch.cuda.stream(side):
+                    with torch.cuda.graph(g, stream=side):
+                        call(0, r, side)
+                cur.wait_stream(side)
+                g.replay()
+                torch.cuda.synchronize()
+                run = g.replay
+            else:
+                def run(mode=mode, r=r):
+                    scratch.zero_()
+                    call(mode, r, torch.cuda.current_stream(dev))
+            best = float("inf")
+            for _ in range(5):
+                if mode != 0:
+                    scratch.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                if mode == 0:
+                    run()
+                else:
+                    call(mode, r, torch.cuda.current_stream(dev))
+                e1.record()
+                e1.synchronize()
+                best = min(best, 1000.0 * e0.elapsed_time(e1))
+            errs = int(scratch[0].item())
+            assert errs == 0, f"{errs} bounded polls gave up in mode {mode}"
+            t[r] = best
+        r0, r1 = rounds
+        out[name] = {"us_per_round": round((t[r1] - t[r0]) / (r1 - r0), 3), "ctas": ctas, "smem_per_cta": smem}
+    return out
 
 
 def isolated_latency(hc, I, dev, pk, reps=200):
@@ -321,6 +389,102 @@ def profile_case(args, hc, I, dev, rows, flags):
                        out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
     torch.cuda.synchronize()
     return {"profile_case": f"decode rows={rows} bf16, 4 weight sets, {args.warmup}+{args.steps} eager blocks"}
+
+
+DOWN_POINTS = ("entry", "weights issued", "dependency wait returned", "S pass done", "inverse RMS ready",
+               "weights landed", "MMA operands ready", "MMA done", "cluster exchange landed", "partial sums written")
+UP_POINTS = ("entry", "prefetches issued", "dependency wait returned", "partial sums landed", "MMA operands ready",
+             "MMA done", "pre-mix products landed", "pre_output written")
+
+
+def phase_report(st, n_down, n_up, blocks):
+    """Reduce phase stamps st[block][kernel][cta][point][gt, clock] (int64) to
+    per-phase durations (ns: SM cycles converted with each CTA's own clock
+    rate) and the hand-offs between the kernels (globaltimer)."""
+    import numpy as np
+    out = {}
+    for kname, k, n, pts, last in (("down", 0, n_down, DOWN_POINTS, 9), ("up", 1, n_up, UP_POINTS, 7)):
+        s = st[blocks, k, :n, :, :].astype(np.float64)          # (blocks, ctas, points, 2)
+        ns_per_cycle = (s[:, :, last, 0] - s[:, :, 0, 0]) / np.maximum(1.0, s[:, :, last, 1] - s[:, :, 0, 1])
+        rows = {}
+        for p in range(1, last + 1):
+            d = (s[:, :, p, 1] - s[:, :, p - 1, 1]) * ns_per_cycle
+            rows[f"{p - 1}->{p} {pts[p]}"] = {"mean_ns": round(float(d.mean()), 1),
+                                              "mean_of_block_max_ns": round(float(d.max(1).mean()), 1)}
+        out[kname] = rows
+        out[f"{kname}_mhz"] = round(float(1e3 / np.median(ns_per_cycle)), 1)
+    gt = st[:, :, :, :, 0].astype(np.float64)
+    down_end = gt[:, 0, :n_down, 9].max(1)
+    down_wait = gt[:, 0, :n_down, 2]
+    up_wait = gt[:, 1, :n_up, 2]
+    up_end = gt[:, 1, :n_up, 7].max(1)
+    b = np.array(blocks)
+    bp = b[b > 0]
+    out["handoff_ns"] = {
+        "down wait returned (first CTA) after the previous block's last up CTA ended":
+            round(float((down_wait[bp].min(1) - up_end[bp - 1]).mean()), 1),
+        "down wait returned (last CTA) after the previous block's last up CTA ended":
+            round(float((down_wait[bp].max(1) - up_end[bp - 1]).mean()), 1),
+        "up wait returned (first CTA) after the last down CTA ended":
+            round(float((up_wait[b].min(1) - down_end[b]).mean()), 1),
+        "up wait returned (last CTA) after the last down CTA ended":
+            round(float((up_wait[b].max(1) - down_end[b]).mean()), 1),
+        "block period (last up CTA end to the next)": round(float((up_end[bp] - up_end[bp - 1]).mean()), 1),
+        "down critical path (last wait return to last end)":
+            round(float((down_end[b] - down_wait[b].max(1)).mean()), 1),
+        "up critical path (last wait return to last end)": round(float((up_end[b] - up_wait[b].max(1)).mean()), 1)}
+    steps = np.diff(np.unique(gt[b, 0, :n_down, :10].ravel()))
+    out["globaltimer_step_ns"] = float(steps[steps > 0].min()) if (steps > 0).any() else None
+    return out
+
+
+def profile_phases(args, hc, I, dev, rows, flags):
+    """Phase clocks of the decode pair (hc_debug_phase_clocks): a 96-block
+    chain over 96 weight sets captured as one CUDA graph with the timed
+    kernels, replayed 5 times; the last replay's stamps are reduced over the
+    steady-state blocks 8..87. The timed kernels compute the same results and
+    add only the stamps; this is a diagnostic, not a benchmark result."""
+    import numpy as np
+    import torch
+    from hyper_connection_rank_gb300 import _binding as B
+    L = B.lib()
+    weights = [I.make_weights(C, H, R, "bf16", seed=0, block=i, device=dev) for i in range(NSETS)]
+    bufs = [I.make_activations(rows, C, H, "bf16", seed=0, block=0, prologue=True, device=dev)]
+    bufs.append({k: torch.empty_like(v) for k, v in bufs[0].items()})
+    ws = torch.empty(max(1, hc.workspace_size(rows, C, H, R, torch.bfloat16, flags)), dtype=torch.uint8, device=dev)
+
+    def step(i):
+        src, dst, w = bufs[i % 2], bufs[(i + 1) % 2], weights[i % NSETS]
+        hc.lowrank_mix(src["streams"], w["norm_scale"], w["down_w"], w["up_w"], w["inject_w"], src["prev_out"],
+                       src["prev_gate"], num_branches=C, flags=flags,
+                       out=(dst["prev_out"], dst["prev_gate"], dst["streams"]), workspace=ws, **QWEN)
+
+    for i in range(4):
+        step(i)
+    torch.cuda.synchronize()
+    slot = L.hc_debug_phase_clocks(None, 0)
+    stamps = torch.zeros(NSETS * slot // 8, dtype=torch.int64, device=dev)
+    L.hc_debug_phase_clocks(stamps.data_ptr(), NSETS * slot)
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream(dev)
+    s.wait_stream(torch.cuda.current_stream(dev))
+    try:
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(NSETS):
+                    step(i)
+    finally:
+        L.hc_debug_phase_clocks(None, 0)
+    torch.cuda.current_stream(dev).wait_stream(s)
+    for _ in range(5):
+        g.replay()
+    torch.cuda.synchronize()
+    st = stamps.view(NSETS, 2, 256, 10, 2).cpu().numpy()
+    n_down = int((st[0, 0, :, 0, 0] != 0).sum())
+    n_up = int((st[0, 1, :, 0, 0] != 0).sum())
+    rep = phase_report(st, n_down, n_up, list(range(8, 88)))
+    return {"profile_case": f"decode phase clocks, rows={rows} bf16, 96-block graph, blocks 8..87 of the last of "
+                            f"5 replays", "ctas": {"down": n_down, "up": n_up}, "phases": rep}
 
 
 def profile_prefill(args, hc, I, dev):
@@ -757,7 +921,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--rows", type=int, default=1, help="decode rows per block (1..8)")
-    ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "prefill", "rowops"),
+    ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "phases", "sync", "prefill", "rowops"),
                     help="small eager case for profiler captures (not a benchmark result)")
     args = ap.parse_args()
     if args.warmup < 3:
