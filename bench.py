@@ -487,20 +487,27 @@ def profile_phases(args, hc, I, dev, rows, flags):
                             f"5 replays", "ctas": {"down": n_down, "up": n_up}, "phases": rep}
 
 
+PREFILL_CONFIGS = {"bf16_c4": ("bf16", 4, 2560), "f16_c8": ("f16", 8, 1280)}
+
+
 def profile_prefill(args, hc, I, dev):
-    """Profiler case for the prefill path: the 8192-row bf16 block (C=4,
-    H=2560, R=320), warmup + steps eager calls through the public API."""
+    """Profiler case for the prefill path: one of the two prefill blocks
+    (--prefill-config: bf16 C=4 H=2560, or fp16 C=8 H=1280; R=320) at
+    --prefill-rows rows (8192 by default), warmup + steps eager calls through
+    the public API."""
     import torch
-    rows = 8192
-    d = I.make_block(rows, C, H, R, "bf16", seed=0, prologue=True, device=dev)
-    ws = torch.empty(hc.workspace_size(rows, C, H, R, torch.bfloat16), dtype=torch.uint8, device=dev)
-    out = (torch.empty(rows, H, dtype=torch.bfloat16, device=dev), torch.empty(rows, C, dtype=torch.bfloat16, device=dev),
-           torch.empty(rows, C * H, dtype=torch.bfloat16, device=dev))
+    dt, Cp, Hp = PREFILL_CONFIGS[args.prefill_config]
+    tdt = {"bf16": torch.bfloat16, "f16": torch.float16}[dt]
+    rows = args.prefill_rows
+    d = I.make_block(rows, Cp, Hp, R, dt, seed=0, prologue=True, device=dev)
+    ws = torch.empty(hc.workspace_size(rows, Cp, Hp, R, tdt), dtype=torch.uint8, device=dev)
+    out = (torch.empty(rows, Hp, dtype=tdt, device=dev), torch.empty(rows, Cp, dtype=tdt, device=dev),
+           torch.empty(rows, Cp * Hp, dtype=tdt, device=dev))
     for _ in range(args.warmup + args.steps):
         hc.lowrank_mix(d["streams"], d["norm_scale"], d["down_w"], d["up_w"], d["inject_w"], d["prev_out"],
-                       d["prev_gate"], num_branches=C, out=out, workspace=ws, **QWEN)
+                       d["prev_gate"], num_branches=Cp, out=out, workspace=ws, **QWEN)
     torch.cuda.synchronize()
-    return {"profile_case": f"prefill rows={rows} bf16, {args.warmup}+{args.steps} eager blocks"}
+    return {"profile_case": f"prefill rows={rows} {dt} C={Cp} H={Hp}, {args.warmup}+{args.steps} eager blocks"}
 
 
 def profile_rowops(args, hc, I, dev):
@@ -921,6 +928,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--rows", type=int, default=1, help="decode rows per block (1..8)")
+    ap.add_argument("--prefill-config", choices=("bf16_c4", "f16_c8"), default="bf16_c4",
+                    help="block of the prefill profile case")
+    ap.add_argument("--prefill-rows", type=int, default=8192, help="rows of the prefill profile case")
     ap.add_argument("--profile-case", nargs="?", const="decode", choices=("decode", "phases", "sync", "prefill", "rowops"),
                     help="small eager case for profiler captures (not a benchmark result)")
     args = ap.parse_args()
