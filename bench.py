@@ -391,7 +391,7 @@ def profile_case(args, hc, I, dev, rows, flags):
     return {"profile_case": f"decode rows={rows} bf16, 4 weight sets, {args.warmup}+{args.steps} eager blocks"}
 
 
-DOWN_POINTS = ("entry", "weights issued", "dependency wait returned", "S pass done", "inverse RMS ready",
+DOWN_POINTS = ("entry", "weights issued", "dependency wait returned", "S pass done", "inverse RMS stored",
                "weights landed", "MMA operands ready", "MMA done", "cluster exchange landed", "partial sums written")
 UP_POINTS = ("entry", "prefetches issued", "dependency wait returned", "partial sums landed", "MMA operands ready",
              "MMA done", "pre-mix products landed", "pre_output written")

@@ -111,7 +111,7 @@ __device__ __forceinline__ void phase_stamp(unsigned long long* rec, int point) 
 // --------------------------------------------------------------- dec_down --
 
 struct DownSmem {
-  uint32_t a, b, wis, ns, ss, wsum, inv, recv, bars, total;
+  uint32_t a, b, wis, ns, ss, wsum, recv, bars, total;
 };
 // A: 2*MT boxes of 64 columns x KS rows; B: ceil(KS/64) blocks. The region
 // starts 1024-aligned (the dynamic shared memory base is aligned by hand).
@@ -124,8 +124,7 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
   L.ns = a16(L.wis + KS * C * 2);
   L.ss = a16(L.ns + KS * 2);       // norm_scale of the slice, T
   L.wsum = a16(L.ss + MB * KS * 2);  // S of the slice, T (already rounded to T: exact)
-  L.inv = a16(L.wsum + nwarps * MB * 4);
-  L.recv = a16(L.inv + MB * 4);
+  L.recv = a16(L.wsum + nwarps * MB * 4);
   L.bars = a16(L.recv + CL * MB * TPR * 32 * 4);
   L.total = L.bars + 32 + 1024;  // barriers, TMEM address; slack for aligning the base
   return L;
@@ -156,9 +155,9 @@ __device__ __forceinline__ uint32_t idesc_t() {
 // registers and the two kernels of a block stop overlapping under PDL,
 // costing 5-6 us per block).
 // Phase points (TIMED): 0 entry, 1 weights issued (before the dependency
-// wait), 2 wait returned, 3 S pass done, 4 inverse RMS ready, 5 weights
-// landed, 6 MMA operands ready, 7 MMA done, 8 cluster exchange landed,
-// 9 partial sums written.
+// wait), 2 wait returned, 3 S pass done (the branch sums of squares in shared
+// memory), 4 inverse RMS stored, 5 weights landed, 6 MMA operands ready, 7 MMA
+// done, 8 cluster exchange landed, 9 partial sums written.
 template <typename T, int MB, bool TIMED = false>
 __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
@@ -175,7 +174,6 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   T* ns_s = reinterpret_cast<T*>(smem + L.ns);
   T* ss = reinterpret_cast<T*>(smem + L.ss);
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
-  float* inv_s = reinterpret_cast<float*>(smem + L.inv);
   float* recv_s = reinterpret_cast<float*>(smem + L.recv);
   uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mma_bar = rbar + 1;
@@ -317,23 +315,32 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   }
   __syncthreads();
   HC_PHASE(3);
-  if (tid < B) {
+  // Every thread forms the inverse RMS of the rows it needs from the warps'
+  // sums itself: the same sum in the same order in every thread, so the same
+  // bits, and no second CTA barrier on the critical path.
+  auto inv_of = [&](int b) {
     float t = 0.0f;
-    for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + tid];
-    const float iv = inv_rms(t, H, a.eps);
-    inv_s[tid] = iv;
-    if (hk0 == 0) a.inv_ws[tid * C + c] = iv;
-  }
-  __syncthreads();
+    for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + b];
+    return inv_rms(t, H, a.eps);
+  };
+  if (hk0 == 0 && tid < B) a.inv_ws[tid * C + c] = inv_of(tid);
   HC_PHASE(4);
   const bool wok = mbar_wait(wbar, 0, &g_um_wait_timeouts);
   HC_PHASE(5);
   // hn of the slice as T, into B at its swizzled position
-  #pragma unroll 1
-  for (int i = tid; i < B * KS; i += nthr) {
-    const int b = i / KS, kk = i - b * KS;
-    *reinterpret_cast<T*>(sB + b_off(b, kk)) =
-        Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(ss[i]), inv_s[b], Ty<T>::to_f(ns_s[kk])));
+  {
+    int b_inv = -1;
+    float iv = 0.0f;
+    #pragma unroll 1
+    for (int i = tid; i < B * KS; i += nthr) {
+      const int b = i / KS, kk = i - b * KS;
+      if (b != b_inv) {
+        iv = inv_of(b);
+        b_inv = b;
+      }
+      *reinterpret_cast<T*>(sB + b_off(b, kk)) =
+          Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(ss[i]), iv, Ty<T>::to_f(ns_s[kk])));
+    }
   }
   place_inject();
   fence_proxy_async_smem();  // generic-proxy writes of A and B, visible to the tensor core
@@ -637,17 +644,27 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       for (int pr = 0; pr < C; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
     }
   }
-  if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
-  #pragma unroll 1
-  for (int i = tid; i < B * HS; i += nthr) {
-    const int b = i / HS, m = i - b * HS;
-    hn_s[i] = Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(hn_s[i]), inv_s[b * C + (m >> lgF)], Ty<T>::to_f(ns_s[m])));
-  }
-  cp_async_wait_all();
+  // The MMA may start once the d warps have written d and hn and every
+  // thread's W_u copies have landed: the last warp only arrives at that
+  // barrier (after its own copies) and then computes the post gate, so the
+  // MMA does not wait for it.
   bool dok = true;
-  if (split) dok = mbar_wait(dbar, 0, &g_um_wait_timeouts);
-  fence_proxy_async_smem();  // A (cp.async) and B (d) visible to the tensor core
-  __syncthreads();
+  if (d_thread) {
+    #pragma unroll 1
+    for (int i = tid; i < B * HS; i += nthr_d) {
+      const int b = i / HS, m = i - b * HS;
+      hn_s[i] = Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(hn_s[i]), inv_s[b * C + (m >> lgF)], Ty<T>::to_f(ns_s[m])));
+    }
+    cp_async_wait_all();
+    if (split) dok = mbar_wait(dbar, 0, &g_um_wait_timeouts);
+    fence_proxy_async_smem();  // A (cp.async) and B (d) visible to the tensor core
+    named_bar_sync(2, static_cast<uint32_t>(nthr));
+  } else {
+    cp_async_wait_all();
+    fence_proxy_async_smem();
+    named_bar_arrive(2, static_cast<uint32_t>(nthr));
+    if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
+  }
   HC_PHASE(4);
 
   // ---- up^T = Wu^T * d^T: the R16/16 k-steps in NI contiguous ranges, range

@@ -192,7 +192,7 @@ hc_status_t hc_debug_sync_probe(int mode, int ctas, int rounds, size_t smem_byte
  * then the up kernel, 256 CTAs x 10 points x {globaltimer ns, SM clock64}
  * (unsigned 64-bit), written by thread 0 of each CTA at the points:
  *   down: 0 entry, 1 weights issued, 2 dependency wait returned, 3 S pass
- *         done, 4 inverse RMS ready, 5 weights landed, 6 MMA operands ready,
+ *         done, 4 inverse RMS stored, 5 weights landed, 6 MMA operands ready,
  *         7 MMA done, 8 cluster exchange landed, 9 partial sums written;
  *   up:   0 entry, 1 prefetches issued, 2 dependency wait returned, 3 partial
  *         sums landed, 4 MMA operands ready, 5 MMA done, 6 pre-mix products
