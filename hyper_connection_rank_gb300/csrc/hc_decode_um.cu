@@ -111,7 +111,7 @@ __device__ __forceinline__ void phase_stamp(unsigned long long* rec, int point) 
 // --------------------------------------------------------------- dec_down --
 
 struct DownSmem {
-  uint32_t a, b, wis, ns, ss, wsum, recv, bars, total;
+  uint32_t a, b, wis, ns, ss, wsum, gs, recv, bars, total;
 };
 // A: 2*MT boxes of 64 columns x KS rows; B: ceil(KS/64) blocks. The region
 // starts 1024-aligned (the dynamic shared memory base is aligned by hand).
@@ -124,9 +124,10 @@ __host__ __device__ inline DownSmem down_smem(int MB, int KS, int R, int C, int 
   L.ns = a16(L.wis + KS * C * 2);
   L.ss = a16(L.ns + KS * 2);       // norm_scale of the slice, T
   L.wsum = a16(L.ss + MB * KS * 2);  // S of the slice, T (already rounded to T: exact)
-  L.recv = a16(L.wsum + nwarps * MB * 4);
+  L.gs = a16(L.wsum + nwarps * MB * 4);  // 32-vector group sums of squares (several rows)
+  L.recv = a16(L.gs + nwarps * MB * 4);
   L.bars = a16(L.recv + CL * MB * TPR * 32 * 4);
-  L.total = L.bars + 32 + 1024;  // barriers, TMEM address; slack for aligning the base
+  L.total = L.bars + 48 + 1024;  // barriers, TMEM address; slack for aligning the base
   return L;
 }
 
@@ -175,10 +176,12 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   T* ss = reinterpret_cast<T*>(smem + L.ss);
   float* wsum = reinterpret_cast<float*>(smem + L.wsum);
   float* recv_s = reinterpret_cast<float*>(smem + L.recv);
+  float* gs = reinterpret_cast<float*>(smem + L.gs);
   uint64_t* rbar = reinterpret_cast<uint64_t*>(smem + L.bars);
   uint64_t* mma_bar = rbar + 1;
   uint64_t* wbar = rbar + 2;  // the slice's weights and norm_scale landed
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 3);
+  uint64_t* xbar = rbar + 3;  // every group sum of squares landed (shared statistic)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rbar + 4);
 
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
@@ -192,12 +195,25 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   // inject columns R..R+C-1: box R/64, 16-byte chunk (R%64)/8
   const int ibox = R / 64, ich = (R % 64) / 8;
   const int nbt = ceil_div(R, 64);  // boxes the W_d copies fill (a ragged last one with zeros)
+  // Shared statistic (three or more rows): the branch's sum of squares of a row
+  // is, at every row count, the sum in group order of G butterfly sums over
+  // 32 consecutive vectors (the warps' sums of the one-pass form, where
+  // thread v takes vector v). With several rows the eight ranks of a cluster
+  // (eight slices of the branch) split the (group, row) pairs, each loading
+  // only its groups' vectors, and send the group sums to every rank: the
+  // same additions in the same order, a fraction of the loads.
+  const int NVr = H / VEC, G = ceil_div(NVr, 32);
+  // (Both forms give the same bits; at two rows the exchange costs more than
+  // the loads it saves, measured 9.75 vs 9.5 us per block.)
+  const bool xmode = MB >= 4 && CL == 8 && NVr <= nthr;
   HC_PHASE(0);
 
   if (tid == 0) {
     mbar_init(rbar, 1);
     mbar_init(mma_bar, MT);  // one commit per tile's issuing warp
     mbar_init(wbar, 1);
+    mbar_init(xbar, 1);
+    mbar_arrive_expect_tx(xbar, xmode ? static_cast<uint32_t>(G * B * 4) : 0u);
     tma_prefetch_desc(&a.tm_wd);
     mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(CL * ncol * B * 4));
     fence_mbar_init();
@@ -261,9 +277,78 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   if (!a.weights_static) issue_weights();
   pdl_trigger();
 
+  bool xok = true;
+  if (xmode) {
+    // ---- shared statistic: (group, row) pair t goes to rank t % 8, warp
+    // t / 8; thread i < B * KS/8 also loads vector i of the slice ----
+    const int NS = KS / VEC, npair = G * B;
+    const int t = warp * 8 + rank;
+    const bool task = t < npair;
+    const int tw = task ? t / B : 0, tb = task ? t - (t / B) * B : 0, tv = tw * 32 + lane;
+    const bool tload = task && tv < NVr;
+    const bool sl = tid < B * NS;
+    const int sb = sl ? tid / NS : 0, sv = sl ? tid - (tid / NS) * NS : 0;
+    uint4 qv = make_uint4(0, 0, 0, 0), qp = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0),
+          lp = make_uint4(0, 0, 0, 0);
+    float qg = 0.0f, lg = 0.0f;
+    if (tload) {
+      qv = ld16(a.streams + tb * CH + static_cast<int64_t>(c) * H + tv * VEC);
+      if (pro) {
+        qp = ld16(a.prev_out + static_cast<int64_t>(tb) * H + tv * VEC);
+        qg = ldf(a.prev_gate + tb * C + c);
+      }
+    }
+    if (sl) {
+      lv = ld16(a.streams + sb * CH + k0 + sv * VEC);
+      if (pro) {
+        lp = ld16(a.prev_out + static_cast<int64_t>(sb) * H + hk0 + sv * VEC);
+        lg = ldf(a.prev_gate + sb * C + c);
+      }
+    }
+    float q = 0.0f;
+    if (tload) {
+      float sf[VEC];
+      V8<T>::unpack(qv, sf);
+      if (pro) {
+        float pf[VEC];
+        V8<T>::unpack(qp, pf);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) sf[j] = prologue_s<T>(sf[j], qg, pf[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < VEC; ++j) q = fmaf(sf[j], sf[j], q);
+    }
+    if (sl) {
+      float sf[VEC];
+      V8<T>::unpack(lv, sf);
+      if (pro) {
+        float pf[VEC];
+        V8<T>::unpack(lp, pf);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) sf[j] = prologue_s<T>(sf[j], lg, pf[j]);
+      }
+      const uint4 sv_t = pro ? V8<T>::pack(sf) : lv;  // S as T (each value already rounded)
+      *reinterpret_cast<uint4*>(ss + sb * KS + sv * VEC) = sv_t;
+      if (a.sout != nullptr) st16(a.sout + sb * CH + k0 + sv * VEC, sv_t);
+    }
+    const float gsum = warp_sum(q);  // the one-pass form's warp sum for group tw
+    cluster_wait();                  // every rank has started: its gs and xbar exist
+    if (task && lane < 8) {
+      const uint32_t slot = smem_addr(gs + tw * MB + tb);
+      st_async_b32(mapa_shared(slot, lane), __float_as_uint(gsum), mapa_shared(smem_addr(xbar), lane));
+    }
+    xok = mbar_wait(xbar, 0, &g_um_wait_timeouts);
+    // each row's inverse RMS, once, from the group sums in group order (the
+    // barrier below publishes it with the slice's S)
+    if (tid < B) {
+      float tsum = 0.0f;
+      for (int w = 0; w < G; ++w) tsum += gs[w * MB + tid];
+      wsum[tid] = inv_rms(tsum, H, a.eps);
+    }
+    __syncthreads();  // the slice's S (ss) and the inverse RMS written by other threads
+  } else {
   // ---- one pass over branch c of every row: S, its sum of squares, the
   // slice's S and streams_out for the slice ----
-  const int NVr = H / VEC;
   float ssq[MB];
 #pragma unroll
   for (int b = 0; b < MB; ++b) ssq[b] = 0.0f;
@@ -314,11 +399,16 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
     if (lane == 0) wsum[warp * MB + b] = w;
   }
   __syncthreads();
+  }
   HC_PHASE(3);
-  // Every thread forms the inverse RMS of the rows it needs from the warps'
-  // sums itself: the same sum in the same order in every thread, so the same
-  // bits, and no second CTA barrier on the critical path.
+  // One row: every thread forms the inverse RMS itself from the warps' sums
+  // (the same sum in the same order in every thread, so the same bits; no
+  // second CTA barrier on the critical path). The shared statistic's sum runs
+  // over the G groups only: the one-pass form's warps past the last group
+  // hold +0, and adding them changes nothing.
+  // (With several rows the statistic of row b is already in wsum[b].)
   auto inv_of = [&](int b) {
+    if (xmode) return wsum[b];
     float t = 0.0f;
     for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + b];
     return inv_rms(t, H, a.eps);
@@ -360,7 +450,7 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
     }
     mma_commit(mma_bar);
   }
-  const bool ok = mbar_wait(mma_bar, 0, &g_um_wait_timeouts) && wok;
+  const bool ok = mbar_wait(mma_bar, 0, &g_um_wait_timeouts) && wok && xok;
   tc_fence_after();
   HC_PHASE(7);
 
@@ -368,7 +458,7 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   // with p % 4 == warp % 4 (a warp reaches only its own lane quarter) and
   // sends row values to the rank that owns the group ----
   const float qnan = __int_as_float(0x7fc00000);
-  cluster_wait();
+  if (!xmode) cluster_wait();
   #pragma unroll 1
   for (int p = warp; p < MT * 4; p += nwarps) {
     const int q = p & 3, mt = p >> 2;
