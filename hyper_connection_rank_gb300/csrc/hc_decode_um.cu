@@ -72,19 +72,19 @@ __host__ __device__ inline uint32_t b_off(int row, int k) { return static_cast<u
 // Workspace position of the cluster-summed partial of column `col` (down
 // columns 0..R-1, then inject columns R..R+7) for row b of cluster p. With
 // one row, (p, b, col) row-major with NCP columns: dec_up_um pulls the whole
-// array with one bulk copy. With more rows (split mode, where up rank c
-// reduces the `per` down columns c*per.. and rank 0 the inject columns) the
+// array with one bulk copy. With more rows (split mode: SR up ranks, rank c
+// reducing the `per` down columns c*per.. and rank 0 the inject columns) the
 // down columns are grouped by the rank that consumes them, (p, rank, b,
 // per), followed by the inject columns as (p, b, 8): each rank pulls one
 // contiguous block per cluster and rank 0 one block of inject columns.
-__host__ __device__ inline int64_t part_index(bool split, int p, int b, int col, int B, int C, int R, int NCP, int per,
-                                              int NCLU) {
-  if (!split) return (static_cast<int64_t>(p) * B + b) * NCP + col;
+// SR = 0 means no split.
+__host__ __device__ inline int64_t part_index(int SR, int p, int b, int col, int B, int R, int NCP, int per, int NCLU) {
+  if (SR == 0) return (static_cast<int64_t>(p) * B + b) * NCP + col;
   if (col < R) {
     const int rank = col / per;
-    return ((static_cast<int64_t>(p) * C + rank) * B + b) * per + (col - rank * per);
+    return ((static_cast<int64_t>(p) * SR + rank) * B + b) * per + (col - rank * per);
   }
-  return static_cast<int64_t>(NCLU) * C * B * per + (static_cast<int64_t>(p) * B + b) * 8 + (col - R);
+  return static_cast<int64_t>(NCLU) * SR * B * per + (static_cast<int64_t>(p) * B + b) * 8 + (col - R);
 }
 
 // Phase clocks (diagnostic, hc_debug_phase_clocks): in the TIMED variants
@@ -138,7 +138,7 @@ struct DownArgs {
   T* sout;
   float* inv_ws;   // (B, C)
   float* part_ws;  // one row: (NCLU, B, NCP), NCP = R + 8; split: see part_index
-  int B, C, H, R, KS, CL, NCP, split, per, NCLU;
+  int B, C, H, R, KS, CL, NCP, split, per, NCLU;  // split: the up ranks SR sharing d, 0 = none
   float eps;
   int weights_static;
   const T* wu;                 // up_w: each CTA prefetches wu_prefetch_bytes of it into L2
@@ -218,7 +218,10 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
     mbar_arrive_expect_tx(rbar, static_cast<uint32_t>(CL * ncol * B * 4));
     fence_mbar_init();
   }
-  if (warp == 1) {
+  // the last warp owns the tensor memory: it frees it as soon as every warp
+  // has read its accumulators, off the path of the warps that still work
+  const int tm_warp = nwarps - 1;
+  if (warp == tm_warp) {
     tmem_alloc(tmem_slot, 64);
     tmem_relinquish();
   }
@@ -477,6 +480,14 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
         }
     }
   }
+  tc_fence_before();
+  if (warp == tm_warp) {
+    named_bar_sync(1, static_cast<uint32_t>(nthr));  // every warp's tensor-memory loads are done
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  } else {
+    named_bar_arrive(1, static_cast<uint32_t>(nthr));
+  }
   const bool rok = mbar_wait(rbar, 0, &g_um_wait_timeouts);
   HC_PHASE(8);
 
@@ -492,14 +503,11 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
 #pragma unroll
     for (int r = 0; r < 8; ++r)
       if (r < CL) t += x[r];
-    a.part_ws[part_index(a.split != 0, cluster_id, b, c_lo + lc, B, C, R, NCP, a.per, a.NCLU)] = rok ? t : qnan;
+    a.part_ws[part_index(a.split, cluster_id, b, c_lo + lc, B, R, NCP, a.per, a.NCLU)] = rok ? t : qnan;
   }
-  tc_fence_before();
-  __syncthreads();
-  HC_PHASE(9);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 64);
+  if constexpr (TIMED) {
+    __syncthreads();
+    HC_PHASE(9);
   }
 }
 
@@ -529,7 +537,7 @@ struct UpArgs {
   const float* inv_ws;
   const float* part_ws;
   T *pre, *post;
-  int B, C, H, R, NCLU, NCP, split, per, st_bytes;
+  int B, C, H, R, NCLU, NCP, split, per, st_bytes;  // split: the cluster size SR, 0 = none
   Attrs at;
   unsigned long long* phase;  // TIMED variants only: [CTA][kPhasePoints][2]
 };
@@ -578,9 +586,10 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar + 4);
 
   // Tile column m (= TMEM lane, = row of A) is feature f0 + m % F of branch
-  // m / F, f0 = blockIdx.x * F. With two or more rows, C consecutive CTAs
+  // m / F, f0 = blockIdx.x * F. With two or more rows, SR consecutive CTAs
   // form a cluster in which rank p reduces share p of the down columns and
-  // broadcasts its part of d (split mode); one row needs no cluster.
+  // broadcasts its part of d (split mode; d is the same for every tile); one
+  // row needs no cluster.
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int f0 = blockIdx.x * F;
@@ -589,6 +598,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   const bool do_post = blockIdx.x == 0;
   // one row needs no split (the host never sets it then): the code is left out
   const bool split = MB > 1 && a.split != 0;
+  const int SR = a.split;
   HC_PHASE(0);
   // The next block's dec_down_um reads nothing before its own dependency wait
   // but static weights (HC_FLAG_WEIGHTS_STATIC), and writes nothing before it:
@@ -602,7 +612,10 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
     mbar_arrive_expect_tx(dbar, split ? static_cast<uint32_t>(R * B * 2) : 0u);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  // a warp with no epilogue work owns the tensor memory and frees it once the
+  // four epilogue warps have read their accumulators
+  const int tm_warp = (nthr >> 5) - 2;
+  if (warp == tm_warp) {
     tmem_alloc(tmem_slot, 64);
     tmem_relinquish();
   }
@@ -688,9 +701,9 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       #pragma unroll 1
       for (int p = lane; p < NCLU; p += 32)
         bulk_g2s(st + static_cast<size_t>(p) * B * a.per,
-                 a.part_ws + (static_cast<int64_t>(p) * C + rank) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
+                 a.part_ws + (static_cast<int64_t>(p) * SR + rank) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
       if (do_post && lane == 0)
-        bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * C * B * a.per,
+        bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * SR * B * a.per,
                  static_cast<uint32_t>(NCLU * B * 32), bar);
     }
   }
@@ -731,7 +744,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       dv[1] = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x1), a.at.alpha) : qnan);
       const uint32_t packed = *reinterpret_cast<const uint32_t*>(dv);
       const uint32_t slot = smem_addr(sB + b_off(b, rank * a.per + lc));  // an even column pair is contiguous
-      for (int pr = 0; pr < C; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
+      for (int pr = 0; pr < SR; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
     }
   }
   // The MMA may start once the d warps have written d and hn and every
@@ -789,6 +802,8 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
 #pragma unroll
     for (int j = 0; j < kUpIssuers; ++j)
       if (j < NI) tmem_ld_wait_r(acc[j]);
+    tc_fence_before();
+    named_bar_arrive(3, 160);
     float v[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -814,12 +829,14 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       stf(a.pre + static_cast<int64_t>(b) * H + f0 + f, __fmul_rn(a.at.rho, acc2));
     }
   }
-  tc_fence_before();
-  __syncthreads();
-  HC_PHASE(7);
-  if (warp == 1) {
+  if (warp == tm_warp) {
+    named_bar_sync(3, 160);  // the four epilogue warps' tensor-memory loads are done
     tc_fence_after();
     tmem_dealloc(tmem, 64);
+  }
+  if constexpr (TIMED) {
+    __syncthreads();
+    HC_PHASE(7);
   }
 }
 
@@ -827,7 +844,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
 
 struct UmCfg {
   bool ok;
-  int KS, NSL, CL, NCLU, NCP, R, down_threads, up_threads;
+  int KS, NSL, CL, NCLU, NCP, H, R, down_threads, up_threads;
 };
 
 int cluster_for(int n) {
@@ -839,12 +856,15 @@ int cluster_for(int n) {
 struct Stage {
   int split, per, bytes;
 };
-Stage stage_for(int64_t rows, int C, int R, int NCLU, int NCP) {
+// From 2 rows on, the up CTAs form clusters of SR (8 where the tile count
+// allows) in which each rank reduces 1/SR of the down columns and broadcasts
+// its part of d: the staging stays small enough for a dec_down_um CTA to
+// share the SM, and each CTA pulls 1/SR of the partial sums.
+Stage stage_for(int64_t rows, int C, int H, int R, int NCLU, int NCP) {
   Stage s;
-  // From 2 rows on each rank reduces 1/C of the columns and broadcasts d: the
-  // staging stays small enough for a dec_down_um CTA to share the SM.
-  s.split = (rows > 1 && C > 1) ? 1 : 0;
-  s.per = ceil_div(ceil_div(R, C), 4) * 4;
+  const int SR = cluster_for((H / kUpHS) * C);
+  s.split = (rows > 1 && SR > 1) ? SR : 0;
+  s.per = s.split ? ceil_div(ceil_div(R, SR), 4) * 4 : 0;
   s.bytes = s.split ? static_cast<int>(NCLU * rows * s.per * 4 + NCLU * rows * 32)
                     : static_cast<int>(NCLU * rows * NCP * 4);
   return s;
@@ -860,6 +880,7 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   if (H % kUpHS != 0 || H > 16384) return g;
   const int CH = C * H;
   g.NCP = R + 8;
+  g.H = H;
   g.R = R;
   g.down_threads = 12 * 32;  // a multiple of 4 warps (TMEM lane quarters)
   g.KS = 0;
@@ -873,10 +894,12 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.NSL = CH / g.KS;
   g.CL = cluster_for(H / g.KS);
   g.NCLU = g.NSL / g.CL;
-  const Stage sg = stage_for(rows, C, R, g.NCLU, g.NCP);
+  const Stage sg = stage_for(rows, C, H, R, g.NCLU, g.NCP);
   if (up_smem(8, R, C, sg.bytes).total > kUmUpCap) return g;
-  // warps for the d columns, plus one more: the post gate's (dec_post_gate)
-  g.up_threads = (std::min(15, std::max(4, ceil_div(R, 32))) + 1) * 32;
+  // warps for the d columns (at least five: the four epilogue warps and the
+  // one that owns the tensor memory), plus one more: the post gate's
+  // (dec_post_gate)
+  g.up_threads = (std::min(15, std::max(5, ceil_div(R, 32))) + 1) * 32;
   g.ok = true;
   return g;
 }
@@ -888,8 +911,8 @@ Layout um_layout(int64_t rows, int C, const UmCfg& g) {
   Layout L;
   L.inv = 0;
   L.part = align_up(static_cast<size_t>(rows) * C * 4, 256);
-  const Stage sg = stage_for(rows, C, g.R, g.NCLU, g.NCP);
-  const size_t nf = sg.split ? static_cast<size_t>(g.NCLU) * rows * (static_cast<size_t>(C) * sg.per + 8)
+  const Stage sg = stage_for(rows, C, g.H, g.R, g.NCLU, g.NCP);
+  const size_t nf = sg.split ? static_cast<size_t>(g.NCLU) * rows * (static_cast<size_t>(sg.split) * sg.per + 8)
                              : static_cast<size_t>(g.NCLU) * rows * g.NCP;
   L.total = align_up(L.part + nf * 4, 256);
   return L;
@@ -941,7 +964,7 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g, unsigned long long* phas
   da.part_ws = part_ws;
   da.B = static_cast<int>(p.rows);
   da.C = p.C; da.H = p.H; da.R = p.R; da.KS = g.KS; da.CL = g.CL; da.NCP = g.NCP; da.NCLU = g.NCLU;
-  const Stage sg = stage_for(p.rows, p.C, p.R, g.NCLU, g.NCP);
+  const Stage sg = stage_for(p.rows, p.C, p.H, p.R, g.NCLU, g.NCP);
   da.split = sg.split; da.per = sg.per;
   da.eps = p.eps;
   da.weights_static = (p.flags & HC_FLAG_WEIGHTS_STATIC) ? 1 : 0;
@@ -974,10 +997,10 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g, unsigned long long* phas
   const size_t usm = up_smem(MB, p.R, p.C, sg.bytes).total;
   e = ensure_smem<dec_up_um<T, MB, TIMED>>(usm);
   if (e != cudaSuccess) return e;
-  // (H / 128) * C tiles of 128 / C features each; clusters of C CTAs only
+  // (H / 128) * C tiles of 128 / C features each; clusters of SR CTAs only
   // where d is split across ranks
   return launch_pdl(dec_up_um<T, MB, TIMED>, dim3((p.H / kUpHS) * p.C), dim3(g.up_threads), usm, p.stream,
-                    static_cast<unsigned>(sg.split ? p.C : 1), ua);
+                    static_cast<unsigned>(sg.split ? sg.split : 1), ua);
 }
 
 template <typename T>
