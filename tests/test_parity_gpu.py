@@ -154,6 +154,18 @@ def test_streams_out_passthrough_and_optional(hc):
     assert none is None and np.array_equal(pre, pre2) and np.array_equal(post, post2)
 
 
+@pytest.mark.parametrize("rows", [300, 700])
+def test_prefill_without_streams_out_bitwise(hc, rows):
+    """With no streams_out requested the prefill path gives pre_output and
+    post_gate the same bits as with it, in both K-split regimes (300 rows:
+    256-wide slices; 700 rows: branch-sized slices)."""
+    d = I.make_block(rows, 4, 2560, 320, "bf16", seed=37, prologue=True)
+    assert hc.path(rows, 4, 2560, 320, torch.bfloat16) == hc.HC_PATH_PREFILL
+    pre, post, sout = run_gpu(hc, d, 4, I.QWEN_ATTRS)
+    pre2, post2, none = run_gpu(hc, d, 4, I.QWEN_ATTRS, want_streams_out=False)
+    assert none is None and np.array_equal(pre, pre2) and np.array_equal(post, post2)
+
+
 def test_zero_up_and_inject_weights(hc):
     d = I.make_block(2, 4, 2560, 320, "bf16", seed=8, prologue=True)
     d["up_w"] = torch.zeros_like(d["up_w"])
