@@ -379,11 +379,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) pf_down(const __grid_constant__
 }
 
 // down = rT(sum of the K-slice partials in slice order) -> ScaledSiLU -> d;
-// inject likewise -> post_gate.
-// One thread per 4 down columns (float4 partial loads, one 8-byte store of d)
-// or per inject column: thread x of a block row handles column group x of
-// row (blockIdx.x * kMidRows + y), R/4 + C <= kMidCols. ScaledSiLU's gate
-// uses the fast sigmoid that matches the accurate one bit for bit on T inputs.
+// inject likewise -> post_gate. ScaledSiLU's gate uses the fast sigmoid that
+// matches the accurate one bit for bit on T inputs.
+//
+// pf_mid: one thread per 4 down columns (float4 partial loads, one 8-byte
+// store of d) or per inject column: thread x of a block row handles column
+// group x of row (blockIdx.x * kMidRows + y), R/4 + C <= kMidCols.
+// MANY (more than eight slices: the 256-wide slices of small batches): the
+// partials of eight slices are loaded before any is added, so that their
+// latencies overlap; they are still added in slice order. With the few
+// branch-sized slices of large batches the plain loop, in a variant with
+// fewer registers, measured faster.
 constexpr int kMidCols = 128, kMidRows = 2;
 template <typename T, bool MANY>
 __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __restrict__ part, int ksplit,
@@ -395,11 +401,6 @@ __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __res
   const int j = threadIdx.x;
   const int64_t row = static_cast<int64_t>(blockIdx.x) * kMidRows + threadIdx.y;
   if (row >= rows || j >= W) return;
-  // MANY (more than eight slices: the 256-wide slices of small batches): the
-  // partials of eight slices are loaded before any is added, so that their
-  // latencies overlap; they are still added in slice order. With the few
-  // branch-sized slices of large batches the plain loop, in a variant with
-  // fewer registers, measured faster.
   if (j < R4) {
     float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!MANY) {
@@ -444,6 +445,43 @@ __global__ void __launch_bounds__(kMidCols * kMidRows) pf_mid(const float* __res
     }
     stf(post + row * C + cc, post_gate_of<T>(rT<T>(t), at.gate_div, at.gate_mul));
   }
+}
+
+// pf_mid_cols: many slices and few rows (up to kMidColsRows). One thread per
+// (row, column) of [down | inject], and up to kMidBatch slices' partials
+// loaded before any is added, so that a column's whole sum costs one L2 round
+// trip instead of five (a warp's loads of a slice are 32 consecutive floats);
+// they are still added in slice order, so the bits are those of pf_mid. No
+// shared memory, so its CTAs start beside pf_down's. (Measured in the bench's
+// chains: 23.9 -> 22.6 us per block at 16 rows, 26.2 -> 25.1 at 64, but 32.4
+// -> 34.1 at 256, where its four times as many load instructions cost more
+// than the round trips they save.)
+constexpr int kMidBatch = 48;
+constexpr int64_t kMidColsRows = 64;
+template <typename T>
+__global__ void __launch_bounds__(256) pf_mid_cols(const float* __restrict__ part, int ksplit, int64_t rows, int R,
+                                                   int C, Attrs at, T* __restrict__ d, T* __restrict__ post) {
+  pdl_wait();
+  pdl_trigger();
+  const int W = R + C, NP = R + 16;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (idx >= rows * W) return;
+  const int64_t row = idx / W;
+  const int col = static_cast<int>(idx - row * W);
+  const float* src = part + row * NP + col;
+  const int64_t sstride = rows * NP;
+  float t = 0.0f;
+  for (int k0 = 0; k0 < ksplit; k0 += kMidBatch) {
+    float p[kMidBatch];
+#pragma unroll
+    for (int i = 0; i < kMidBatch; ++i)
+      if (k0 + i < ksplit) p[i] = src[(k0 + i) * sstride];
+#pragma unroll
+    for (int i = 0; i < kMidBatch; ++i)
+      if (k0 + i < ksplit) t += p[i];
+  }
+  if (col < R) stf(d + row * R + col, scaled_silu_t<T>(rT<T>(t), at.alpha));
+  else stf(post + row * C + (col - R), post_gate_of<T>(rT<T>(t), at.gate_div, at.gate_mul));
 }
 
 // Persistent up projection. A tile is 128 rows x 64 features; its C branches
@@ -976,10 +1014,15 @@ cudaError_t run_prefill(const Problem& p) {
   if (e != cudaSuccess) return e;
 
   const Attrs at{p.eps, p.rho, p.alpha, p.gate_div, p.gate_mul};
-  e = launch_pdl(ksplit > 8 ? pf_mid<T, true> : pf_mid<T, false>, dim3(static_cast<unsigned>((rows + kMidRows - 1) / kMidRows)), dim3(kMidCols, kMidRows), 0,
-                 p.stream, 1u,
-                 static_cast<const float*>(part), static_cast<int>(ksplit), rows, R, C, at, d,
-                 static_cast<T*>(p.post_gate));
+  if (ksplit > 8 && rows <= kMidColsRows)
+    e = launch_pdl(pf_mid_cols<T>, dim3(static_cast<unsigned>((rows * (R + C) + 255) / 256)), dim3(256), 0, p.stream,
+                   1u, static_cast<const float*>(part), static_cast<int>(ksplit), rows, R, C, at, d,
+                   static_cast<T*>(p.post_gate));
+  else
+    e = launch_pdl(ksplit > 8 ? pf_mid<T, true> : pf_mid<T, false>,
+                   dim3(static_cast<unsigned>((rows + kMidRows - 1) / kMidRows)), dim3(kMidCols, kMidRows), 0,
+                   p.stream, 1u, static_cast<const float*>(part), static_cast<int>(ksplit), rows, R, C, at, d,
+                   static_cast<T*>(p.post_gate));
   if (e != cudaSuccess) return e;
 
   PfUpArgs<T> ua;

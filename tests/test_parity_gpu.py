@@ -154,6 +154,20 @@ def test_streams_out_passthrough_and_optional(hc):
     assert none is None and np.array_equal(pre, pre2) and np.array_equal(post, post2)
 
 
+def test_prefill_mid_reduction_variants_same_bits(hc):
+    """Batches of up to 64 rows sum the K-slice partials with one thread per
+    column, larger ones with one per four columns: the same additions in the
+    same order, so the rows of a 40-row call equal the same rows of a 100-row
+    call bit for bit."""
+    C, H, R = 4, 2560, 320
+    d = I.make_block(100, C, H, R, "bf16", seed=41, prologue=True)
+    full = run_gpu(hc, d, C, I.QWEN_ATTRS)
+    sub = {k: (v[30:70] if k in ("streams", "prev_out", "prev_gate") else v) for k, v in d.items()}
+    part = run_gpu(hc, sub, C, I.QWEN_ATTRS)
+    for a, b in zip(full, part):
+        assert np.array_equal(a[30:70], b)
+
+
 @pytest.mark.parametrize("rows", [300, 700])
 def test_prefill_without_streams_out_bitwise(hc, rows):
     """With no streams_out requested the prefill path gives pre_output and
