@@ -47,6 +47,7 @@ namespace {
 
 constexpr int kUmRowsN = 16;    // MMA N: activation rows, padded
 constexpr int kUmMaxMT = 4;     // dec_down: at most 4 tiles of 128 columns (R + 8 <= 512)
+constexpr int kDownWarps = 12;  // dec_down: 384 threads, a multiple of 4 warps (TMEM lane quarters)
 constexpr int kUpHS = 128;      // dec_up: output columns per CTA (one M tile: C branches x 128/C features)
 constexpr int kUpIssuers = 4;   // dec_up: issuing warps = accumulators
 constexpr int kKBlock = 2048;   // one 64-k block of B: 16 rows x 128 bytes
@@ -413,15 +414,40 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   auto inv_of = [&](int b) {
     if (xmode) return wsum[b];
     float t = 0.0f;
-    for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + b];
+    if constexpr (MB <= 2) {
+      float x[kDownWarps];  // blockDim.x == kDownWarps * 32
+#pragma unroll
+      for (int w = 0; w < kDownWarps; ++w) x[w] = wsum[w * MB + b];  // all loads in flight, then the sum in order
+#pragma unroll
+      for (int w = 0; w < kDownWarps; ++w) t += x[w];
+    } else {
+      #pragma unroll 1
+      for (int w = 0; w < nwarps; ++w) t += wsum[w * MB + b];
+    }
     return inv_rms(t, H, a.eps);
   };
-  if (hk0 == 0 && tid < B) a.inv_ws[tid * C + c] = inv_of(tid);
+  // One or two rows: the inverse RMS once per thread, before the weights are
+  // waited for, and one thread per K row of the slice for hn (no division)
+  float inv2[2] = {0.0f, 0.0f};
+  if constexpr (MB <= 2) {
+    inv2[0] = inv_of(0);
+    if (MB == 2 && B == 2) inv2[1] = inv_of(1);
+  }
+  if (hk0 == 0 && tid < B) a.inv_ws[tid * C + c] = MB <= 2 ? (tid == 0 ? inv2[0] : inv2[1]) : inv_of(tid);
   HC_PHASE(4);
   const bool wok = mbar_wait(wbar, 0, &g_um_wait_timeouts);
   HC_PHASE(5);
   // hn of the slice as T, into B at its swizzled position
-  {
+  if constexpr (MB <= 2) {
+    if (tid < KS) {
+      const float nsv = Ty<T>::to_f(ns_s[tid]);
+#pragma unroll
+      for (int b = 0; b < MB; ++b)
+        if (b < B)
+          *reinterpret_cast<T*>(sB + b_off(b, tid)) =
+              Ty<T>::from_f(norm_hn<T>(Ty<T>::to_f(ss[b * KS + tid]), inv2[b], nsv));
+    }
+  } else {
     int b_inv = -1;
     float iv = 0.0f;
     #pragma unroll 1
@@ -882,7 +908,7 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.NCP = R + 8;
   g.H = H;
   g.R = R;
-  g.down_threads = 12 * 32;  // a multiple of 4 warps (TMEM lane quarters)
+  g.down_threads = kDownWarps * 32;
   g.KS = 0;
   for (int ks = 16; ks <= std::min(H, 256); ks += 16) {  // KS rows: one tensor-copy box (at most 256)
     if (H % ks != 0) continue;
