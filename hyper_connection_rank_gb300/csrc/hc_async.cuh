@@ -163,16 +163,16 @@ __device__ __forceinline__ void st_async_b32(uint32_t raddr, uint32_t v, uint32_
 
 // v(0) + v(1) + ... + v(n-1) added in that order, with the loads behind v
 // issued eight at a time so their latencies overlap.
-template <class F>
+template <int NB = 8, class F>
 __device__ __forceinline__ float ordered_sum(int n, F v) {
   float t = 0.0f;
   int p = 0;
-  for (; p + 8 <= n; p += 8) {
-    float x[8];
+  for (; p + NB <= n; p += NB) {
+    float x[NB];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) x[j] = v(p + j);
+    for (int j = 0; j < NB; ++j) x[j] = v(p + j);
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t += x[j];
+    for (int j = 0; j < NB; ++j) t += x[j];
   }
   for (; p < n; ++p) t += v(p);
   return t;

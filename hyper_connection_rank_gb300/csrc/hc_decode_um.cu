@@ -733,10 +733,12 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
                  static_cast<uint32_t>(NCLU * B * 32), bar);
     }
   }
-  // the inverse RMS of every (row, branch), from dec_down_um, while the
-  // partial sums travel
-  for (int i = tid; i < B * C; i += nthr) inv_s[i] = a.inv_ws[i];
+  // the inverse RMS of every (row, branch), from dec_down_um: its load is
+  // issued before the wait for the partial sums, so the two latencies
+  // overlap (B * C <= 64 < nthr)
+  const float inv_ld = tid < B * C ? a.inv_ws[tid] : 0.0f;
   const bool ok = mbar_wait(bar, 0, &g_um_wait_timeouts);
+  if (tid < B * C) inv_s[tid] = inv_ld;
   cp_async_wait_group1();  // this thread's norm_scale chunk landed (the W_u copies may still fly)
   __syncthreads();
   const float qnan = __int_as_float(0x7fc00000);
