@@ -816,14 +816,17 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   tc_fence_after();
   HC_PHASE(5);
 
-  // ---- epilogue: warp w < 4 holds tile columns 32w..32w+31 (its TMEM lane
-  // quarter), rows in TMEM columns: g = rT(sigmoid(rT(up))) and hn*g go to
-  // shared memory; then each feature's C products are summed in branch order
-  // (the pre-mix) and scaled into pre_output ----
-  if (warp < 4) {
+  // ---- epilogue: warp w < EW holds tile columns 32(w%4)..+31 (its TMEM
+  // lane quarter), rows in TMEM columns; with four rows or more two warps
+  // share a lane quarter, each taking every other row: g =
+  // rT(sigmoid(rT(up))) and hn*g go to shared memory; then each feature's C
+  // products are summed in branch order (the pre-mix) and scaled into
+  // pre_output ----
+  constexpr int EW = MB >= 4 ? 8 : 4, RS = EW / 4;
+  if (warp < EW) {
     // accumulators 0..NI-1 of this lane quarter, added as ((a0 + a1) + (a2 + a3))
     uint32_t acc[kUpIssuers][16];
-    const uint32_t tq = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    const uint32_t tq = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
 #pragma unroll
     for (int j = 0; j < kUpIssuers; ++j)
       if (j < NI) tmem_ld16_nowait(tq + j * kUmRowsN, acc[j]);
@@ -831,7 +834,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
     for (int j = 0; j < kUpIssuers; ++j)
       if (j < NI) tmem_ld_wait_r(acc[j]);
     tc_fence_before();
-    named_bar_arrive(3, 160);
+    named_bar_arrive(3, 32 * EW + 32);
     float v[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -840,17 +843,17 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
       for (int j = 0; j < kUpIssuers; ++j) x[j] = j < NI ? __uint_as_float(acc[j][r]) : 0.0f;
       v[r] = __fadd_rn(__fadd_rn(x[0], x[1]), __fadd_rn(x[2], x[3]));
     }
-    const int m = warp * 32 + lane;
+    const int m = (warp & 3) * 32 + lane, rh = warp >> 2;
 #pragma unroll
     for (int b = 0; b < MB; ++b)
-      if (b < B) {
+      if (b < B && b % RS == rh) {
         const float gg = sigmoid_rT<T>(rT<T>(v[b]));
         mix_s[b * HS + m] = (dok && mmok) ? __fmul_rn(Ty<T>::to_f(hn_s[b * HS + m]), gg) : qnan;
       }
-    named_bar_sync(1, 128);  // the four epilogue warps
+    named_bar_sync(1, 32 * EW);  // the epilogue warps
     HC_PHASE(6);
     #pragma unroll 1
-    for (int i = tid; i < B * F; i += 128) {
+    for (int i = tid; i < B * F; i += 32 * EW) {
       const int b = i / F, f = i - b * F;
       float acc2 = 0.0f;
       for (int cb = 0; cb < C; ++cb) acc2 = __fadd_rn(acc2, mix_s[b * HS + cb * F + f]);
@@ -858,7 +861,7 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
     }
   }
   if (warp == tm_warp) {
-    named_bar_sync(3, 160);  // the four epilogue warps' tensor-memory loads are done
+    named_bar_sync(3, 32 * EW + 32);  // the epilogue warps' tensor-memory loads are done
     tc_fence_after();
     tmem_dealloc(tmem, 64);
   }
@@ -924,10 +927,10 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.NCLU = g.NSL / g.CL;
   const Stage sg = stage_for(rows, C, H, R, g.NCLU, g.NCP);
   if (up_smem(8, R, C, sg.bytes).total > kUmUpCap) return g;
-  // warps for the d columns (at least five: the four epilogue warps and the
-  // one that owns the tensor memory), plus one more: the post gate's
+  // warps for the d columns (at least nine: up to eight epilogue warps and
+  // the one that owns the tensor memory), plus one more: the post gate's
   // (dec_post_gate)
-  g.up_threads = (std::min(15, std::max(5, ceil_div(R, 32))) + 1) * 32;
+  g.up_threads = (std::min(15, std::max(9, ceil_div(R, 32))) + 1) * 32;
   g.ok = true;
   return g;
 }
