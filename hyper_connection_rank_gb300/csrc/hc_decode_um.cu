@@ -817,12 +817,13 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
   HC_PHASE(5);
 
   // ---- epilogue: warp w < EW holds tile columns 32(w%4)..+31 (its TMEM
-  // lane quarter), rows in TMEM columns; with four rows or more two warps
-  // share a lane quarter, each taking every other row: g =
+  // lane quarter), rows in TMEM columns; with two rows or more two warps
+  // share a lane quarter, each taking every other row (three warps measured
+  // slower at eight rows, 11.44 vs 11.38 us per block): g =
   // rT(sigmoid(rT(up))) and hn*g go to shared memory; then each feature's C
   // products are summed in branch order (the pre-mix) and scaled into
   // pre_output ----
-  constexpr int EW = MB >= 4 ? 8 : 4, RS = EW / 4;
+  constexpr int EW = MB >= 2 ? 8 : 4, RS = EW / 4;
   if (warp < EW) {
     // accumulators 0..NI-1 of this lane quarter, added as ((a0 + a1) + (a2 + a3))
     uint32_t acc[kUpIssuers][16];
