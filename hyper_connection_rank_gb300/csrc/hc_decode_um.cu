@@ -47,6 +47,7 @@ namespace {
 
 constexpr int kUmRowsN = 16;    // MMA N: activation rows, padded
 constexpr int kUmMaxMT = 4;     // dec_down: at most 4 tiles of 128 columns (R + 8 <= 512)
+constexpr int kDownClusterMax = 16;  // dec_down: largest cluster (16 is a non-portable size)
 constexpr int kDownWarps = 12;  // dec_down: 384 threads, a multiple of 4 warps (TMEM lane quarters)
 constexpr int kUpHS = 128;      // dec_up: output columns per CTA (one M tile: C branches x 128/C features)
 constexpr int kUpIssuers = 4;   // dec_up: issuing warps = accumulators
@@ -206,7 +207,7 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   const int NVr = H / VEC, G = ceil_div(NVr, 32);
   // (Both forms give the same bits; at two rows the exchange costs more than
   // the loads it saves, measured 9.75 vs 9.5 us per block.)
-  const bool xmode = MB >= 4 && CL == 8 && NVr <= nthr;
+  const bool xmode = MB >= 4 && CL >= 8 && NVr <= nthr;
   HC_PHASE(0);
 
   if (tid == 0) {
@@ -283,10 +284,10 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
 
   bool xok = true;
   if (xmode) {
-    // ---- shared statistic: (group, row) pair t goes to rank t % 8, warp
-    // t / 8; thread i < B * KS/8 also loads vector i of the slice ----
+    // ---- shared statistic: (group, row) pair t goes to rank t % CL, warp
+    // t / CL; thread i < B * KS/8 also loads vector i of the slice ----
     const int NS = KS / VEC, npair = G * B;
-    const int t = warp * 8 + rank;
+    const int t = warp * CL + rank;
     const bool task = t < npair;
     const int tw = task ? t / B : 0, tb = task ? t - (t / B) * B : 0, tv = tw * 32 + lane;
     const bool tload = task && tv < NVr;
@@ -337,7 +338,7 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
     }
     const float gsum = warp_sum(q);  // the one-pass form's warp sum for group tw
     cluster_wait();                  // every rank has started: its gs and xbar exist
-    if (task && lane < 8) {
+    if (task && lane < CL) {
       const uint32_t slot = smem_addr(gs + tw * MB + tb);
       st_async_b32(mapa_shared(slot, lane), __float_as_uint(gsum), mapa_shared(smem_addr(xbar), lane));
     }
@@ -522,12 +523,12 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   #pragma unroll 1
   for (int i = tid; i < B * ncol; i += nthr) {
     const int b = i / ncol, lc = i - b * ncol;
-    float x[8];
+    float x[kDownClusterMax];
 #pragma unroll
-    for (int r = 0; r < 8; ++r) x[r] = r < CL ? recv_s[(r * MB + b) * OC + lc] : 0.0f;
+    for (int r = 0; r < kDownClusterMax; ++r) x[r] = r < CL ? recv_s[(r * MB + b) * OC + lc] : 0.0f;
     float t = 0.0f;
 #pragma unroll
-    for (int r = 0; r < 8; ++r)
+    for (int r = 0; r < kDownClusterMax; ++r)
       if (r < CL) t += x[r];
     a.part_ws[part_index(a.split, cluster_id, b, c_lo + lc, B, R, NCP, a.per, a.NCLU)] = rok ? t : qnan;
   }
@@ -885,6 +886,11 @@ int cluster_for(int n) {
   return 1;
 }
 
+// dec_down_um's clusters: 16 slices of a branch where they divide it (a
+// non-portable cluster size, allowed on the kernel before its launch), else
+// as cluster_for
+int down_cluster_for(int n) { return (kDownClusterMax >= 16 && n % 16 == 0) ? 16 : cluster_for(n); }
+
 struct Stage {
   int split, per, bytes;
 };
@@ -918,13 +924,13 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.KS = 0;
   for (int ks = 16; ks <= std::min(H, 256); ks += 16) {  // KS rows: one tensor-copy box (at most 256)
     if (H % ks != 0) continue;
-    if (down_smem(8, ks, R, C, cluster_for(H / ks), g.down_threads / 32).total > kUmDownCap) break;
+    if (down_smem(8, ks, R, C, down_cluster_for(H / ks), g.down_threads / 32).total > kUmDownCap) break;
     g.KS = ks;
     if (CH / ks <= num_sms) break;
   }
   if (g.KS == 0) return g;
   g.NSL = CH / g.KS;
-  g.CL = cluster_for(H / g.KS);
+  g.CL = down_cluster_for(H / g.KS);
   g.NCLU = g.NSL / g.CL;
   const Stage sg = stage_for(rows, C, H, R, g.NCLU, g.NCP);
   if (up_smem(8, R, C, sg.bytes).total > kUmUpCap) return g;
@@ -1007,6 +1013,8 @@ cudaError_t run_um_mb(const Problem& p, const UmCfg& g, unsigned long long* phas
   da.wu_prefetch_bytes = static_cast<uint32_t>((static_cast<size_t>(p.R) * p.C * p.H * sizeof(T) / g.NSL) & ~size_t{15});
   const size_t dsm = down_smem(MB, g.KS, p.R, p.C, g.CL, g.down_threads / 32).total;
   cudaError_t e = ensure_smem<dec_down_um<T, MB, TIMED>>(dsm);
+  if (e == cudaSuccess && g.CL > 8)
+    e = cudaFuncSetAttribute(dec_down_um<T, MB, TIMED>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e != cudaSuccess) return e;
   e = launch_pdl(dec_down_um<T, MB, TIMED>, dim3(g.NSL), dim3(g.down_threads), dsm, p.stream,
                  static_cast<unsigned>(g.CL), da);
