@@ -1,4 +1,4 @@
-// Decode path for fp16 / bf16 I/O (rows <= 8) with both projections on the
+// Decode path for fp16 / bf16 I/O (rows <= 16) with both projections on the
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory).
 //
 // Same block and the same two-kernel structure as hc_decode_tc.cu (split-K
@@ -54,6 +54,8 @@ constexpr int kUpHS = 128;      // dec_up: output columns per CTA (one M tile: C
 constexpr int kUpIssuers = 4;   // dec_up: issuing warps = accumulators
 constexpr int kKBlock = 2048;   // one 64-k block of B: 16 rows x 128 bytes
 constexpr size_t kUmDownCap = 120 * 1024, kUmUpCap = 150 * 1024;
+constexpr size_t kUmSmPerSm = 233472;  // shared memory of an SM (228 KB)
+constexpr int kUmMaxRows = 16;         // rows of one call: the MMA's N
 
 __host__ __device__ inline uint32_t a16(uint32_t x) { return (x + 15u) & ~15u; }
 __host__ __device__ inline uint32_t a1024(uint32_t x) { return (x + 1023u) & ~1023u; }
@@ -208,7 +210,7 @@ __global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> 
   const int NVr = H / VEC, G = ceil_div(NVr, 32);
   // (Both forms give the same bits; at two rows the exchange costs more than
   // the loads it saves, measured 9.75 vs 9.5 us per block.)
-  const bool xmode = MB >= 4 && CL >= 8 && NVr <= nthr;
+  const bool xmode = MB >= 4 && CL >= 8 && NVr <= nthr && G * B <= nwarps * CL;
   HC_PHASE(0);
 
   if (tid == 0) {
@@ -588,6 +590,24 @@ __device__ __noinline__ void dec_post_gate(const float* st, size_t inj_off, bool
   }
 }
 
+// The same at 9-16 rows, where no CTA stages the inject partials: they are
+// read from the workspace (inj: row 0 of cluster 0, rows 8 and clusters
+// 8 * B floats apart). (One function serving both, with its source pointer
+// chosen by the caller, measured 0.1-0.2 us per block slower at 2-8 rows.)
+template <typename T>
+__device__ __noinline__ void dec_post_gate_ws(const float* inj, int B, int C, int NCLU, bool ok, T* post,
+                                              float gate_div, float gate_mul) {
+  const float qnan = __int_as_float(0x7fc00000);
+  #pragma unroll 1
+  for (int i = static_cast<int>(threadIdx.x) - static_cast<int>(blockDim.x - 32); i >= 0 && i < B * C; i += 32) {
+    const int b = i / C, cc = i - b * C;
+    const float* src = inj + static_cast<size_t>(b) * 8 + cc;
+    const size_t stride = static_cast<size_t>(B) * 8;
+    const float x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
+    stf(post + b * C + cc, ok ? post_gate_of<T>(rT<T>(x), gate_div, gate_mul) : qnan);
+  }
+}
+
 // Phase points (TIMED): 0 entry, 1 prefetches issued (before the dependency
 // wait), 2 wait returned, 3 partial sums landed, 4 MMA operands ready, 5 MMA
 // done, 6 pre-mix products landed, 7 pre_output written.
@@ -714,23 +734,28 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
 
   // ---- pull the down partials into shared memory ----
   const int ncols = split ? max(0, min(R, (rank + 1) * a.per) - rank * a.per) : 0;
+  // up to 8 rows, CTA 0 also stages every cluster's inject partials for the
+  // post gate; at 9-16 rows they stay in the workspace (the post gate reads
+  // them there) to leave room for a dec_down_um CTA beside this one
+  constexpr bool kStageInj = MB <= 8;
   const size_t inj_off = static_cast<size_t>(NCLU) * B * a.per;  // floats (split layout)
   if (warp == 0) {
     uint32_t bytes;
     if (!split) bytes = static_cast<uint32_t>(NCLU * B * NCP * 4);
-    else bytes = static_cast<uint32_t>(NCLU * B * a.per * 4 + (do_post ? NCLU * B * 32 : 0));
+    else bytes = static_cast<uint32_t>(NCLU * B * a.per * 4 + (kStageInj && do_post ? NCLU * B * 32 : 0));
     if (lane == 0) mbar_arrive_expect_tx(bar, bytes);
     __syncwarp();
     if (!split) {
       if (lane == 0) bulk_g2s(st, a.part_ws, bytes, bar);
     } else {
       // one block of B * per partials per cluster for this rank, and (rank 0
-      // of the first column tile) one block of every cluster's inject partials
+      // of the first column tile, up to 8 rows) one block of every cluster's
+      // inject partials
       #pragma unroll 1
       for (int p = lane; p < NCLU; p += 32)
         bulk_g2s(st + static_cast<size_t>(p) * B * a.per,
                  a.part_ws + (static_cast<int64_t>(p) * SR + rank) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
-      if (do_post && lane == 0)
+      if (kStageInj && do_post && lane == 0)
         bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * SR * B * a.per,
                  static_cast<uint32_t>(NCLU * B * 32), bar);
     }
@@ -796,7 +821,13 @@ __global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
     cp_async_wait_all();
     fence_proxy_async_smem();
     named_bar_arrive(2, static_cast<uint32_t>(nthr));
-    if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
+    if constexpr (kStageInj) {
+      if (do_post) dec_post_gate<T>(st, inj_off, split, B, C, NCLU, NCP, R, ok, a.post, a.at.gate_div, a.at.gate_mul);
+    } else {
+      if (do_post)
+        dec_post_gate_ws<T>(a.part_ws + static_cast<size_t>(NCLU) * SR * B * a.per, B, C, NCLU, ok, a.post,
+                            a.at.gate_div, a.at.gate_mul);
+    }
   }
   HC_PHASE(4);
 
@@ -938,7 +969,7 @@ Stage stage_for(int64_t rows, int C, int H, int R, int NCLU, int NCP) {
   const int SR = cluster_for((H / kUpHS) * C);
   s.split = (rows > 1 && SR > 1) ? SR : 0;
   s.per = s.split ? ceil_div(ceil_div(R, SR), 4) * 4 : 0;
-  s.bytes = s.split ? static_cast<int>(NCLU * rows * s.per * 4 + NCLU * rows * 32)
+  s.bytes = s.split ? static_cast<int>(NCLU * rows * s.per * 4 + (rows <= 8 ? NCLU * rows * 32 : 0))
                     : static_cast<int>(NCLU * rows * NCP * 4);
   return s;
 }
@@ -947,7 +978,7 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   UmCfg g{};
   g.ok = false;
   if (dt != HC_F16 && dt != HC_BF16) return g;
-  if (rows < 1 || rows > 8) return g;
+  if (rows < 1 || rows > kUmMaxRows) return g;
   if (!(C == 1 || C == 2 || C == 4 || C == 8)) return g;
   if (R < 16 || R % 8 != 0 || R + 8 > kUmMaxMT * 128) return g;
   if (H % kUpHS != 0 || H > 16384) return g;
@@ -969,6 +1000,16 @@ UmCfg um_cfg(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms) {
   g.NCLU = g.NSL / g.CL;
   const Stage sg = stage_for(rows, C, H, R, g.NCLU, g.NCP);
   if (up_smem(8, R, C, sg.bytes).total > kUmUpCap) return g;
+  if (rows > 8) {
+    // 9-16 rows: only where a CTA of each kernel still fits one SM together
+    // (1 KB of each CTA's shared memory is reserved), so the next kernel's
+    // CTAs start beside the running ones; the K slices are the same as at
+    // eight rows, so a row's bits do not depend on the row count
+    // (decided at 16 rows, so the decode/prefill switch of a shape is at 8 or 16 rows)
+    const size_t dsm = down_smem(16, g.KS, R, C, g.CL, g.down_threads / 32).total;
+    const size_t usm = up_smem(16, R, C, stage_for(16, C, H, R, g.NCLU, g.NCP).bytes).total;
+    if (dsm > kUmDownCap || usm > kUmUpCap || dsm + usm + 2048 > kUmSmPerSm) return g;
+  }
   // warps for the d columns (at least nine: up to eight epilogue warps and
   // the one that owns the tensor memory), plus one more: the post gate's
   // (dec_post_gate)
@@ -1083,7 +1124,8 @@ cudaError_t run_um(const Problem& p, const UmCfg& g) {
   if (p.rows <= 1) return run_um_mb<T, 1>(p, g);
   if (p.rows <= 2) return run_um_mb<T, 2>(p, g);
   if (p.rows <= 4) return run_um_mb<T, 4>(p, g);
-  return run_um_mb<T, 8>(p, g);
+  if (p.rows <= 8) return run_um_mb<T, 8>(p, g);
+  return run_um_mb<T, 16>(p, g);
 }
 
 }  // namespace

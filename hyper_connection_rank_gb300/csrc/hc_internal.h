@@ -36,7 +36,7 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t general_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 cudaError_t launch_general(const Problem& p);
 
-// Decode path: rows <= 8, split-K weight streaming (hc_decode.cu).
+// Decode path: rows <= 8 (16 for the tcgen05 pair), split-K weight streaming (hc_decode.cu).
 bool decode_supported(int64_t rows, int C, int H, int R, hc_dtype_t dt);
 size_t decode_workspace(int64_t rows, int C, int H, int R, hc_dtype_t dt, int num_sms);
 cudaError_t launch_decode(const Problem& p);

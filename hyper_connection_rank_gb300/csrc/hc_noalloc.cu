@@ -12,10 +12,12 @@
 // Limits and sharing:
 //   * the scratch is kHcStaticScratchBytes (1 MiB) per GPU, held from the
 //     first load of the library until the process exits;
-//   * only decode-path problems fit: rows <= 8, all pointers 16-byte aligned,
-//     and a partial-sum buffer that fits in 1 MiB (the 4 x 2560, rank-320
-//     block needs about 210 KB at 8 rows); anything else returns
-//     HC_ERR_UNSUPPORTED with a message in hc_last_error();
+//   * only decode-path problems fit (up to 8 rows, or 16 where the
+//     tensor-core pair serves them; hc_lowrank_mix_path says which), all
+//     pointers 16-byte aligned, and a partial-sum buffer that fits in 1 MiB
+//     (the 4 x 2560, rank-320 block needs well under 200 KB at 16 rows);
+//     anything else returns HC_ERR_UNSUPPORTED with a message in
+//     hc_last_error();
 //   * every call uses the same array, which keeps whatever the last call left
 //     there. The decode kernels write every scratch word they read within one
 //     call, so nothing needs clearing, but two calls whose kernels can run at
@@ -82,7 +84,8 @@ extern "C" hc_status_t hc_lowrank_mix_decode_noalloc(
   if (path != HC_PATH_DECODE || !aligned)
     return hc::set_error(HC_ERR_UNSUPPORTED,
                          "the allocation-free entry point serves decode-path problems only "
-                         "(rows <= 8, C in {1,2,4,8}, H %% 16 == 0, R %% 8 == 0, R <= 512, 16-byte aligned pointers)");
+                         "(hc_lowrank_mix_path gives HC_PATH_DECODE: up to 8 rows, or 16 for the tensor-core pair's "
+                         "shapes; 16-byte aligned pointers)");
   int dev = 0, num_sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev);

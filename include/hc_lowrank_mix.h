@@ -74,7 +74,7 @@ typedef struct {
 
 /* Path selected for a call (hc_lowrank_mix_path). */
 #define HC_PATH_NONE 0    /* rows == 0: nothing is launched */
-#define HC_PATH_DECODE 1  /* rows <= 8: split-K weight-streaming GEMV pair */
+#define HC_PATH_DECODE 1  /* rows <= 8 (16 for the bf16/fp16 tensor-core pair): split-K weight-streaming pair */
 #define HC_PATH_PREFILL 2 /* many rows, fp16/bf16: tcgen05 tensor-core contractions */
 #define HC_PATH_GENERAL 3 /* any shape, any rows, any T: CUDA-core kernels */
 
@@ -133,10 +133,11 @@ hc_status_t hc_lowrank_mix(const void* streams, const void* norm_scale, const vo
  * allocates nothing.
  *
  * Arguments and outputs are those of hc_lowrank_mix without the workspace.
- * Only decode-path problems fit (rows <= 8, C in {1,2,4,8}, H % 16 == 0,
- * R % 8 == 0, R <= 512, every pointer 16-byte aligned, partial sums within
- * 1 MiB; the 4 x 2560, rank-320 block uses about 210 KB at 8 rows); anything
- * else returns HC_ERR_UNSUPPORTED with the reason in hc_last_error().
+ * Only decode-path problems fit (hc_lowrank_mix_path gives HC_PATH_DECODE:
+ * up to 8 rows, or 16 for the bf16/fp16 tensor-core pair's shapes), every
+ * pointer 16-byte aligned, partial sums within 1 MiB (the 4 x 2560, rank-320
+ * block uses well under 200 KB at 16 rows); anything else returns
+ * HC_ERR_UNSUPPORTED with the reason in hc_last_error().
  * All calls share the one array and it keeps the last call's contents (the
  * kernels need no cleared scratch); calls whose kernels may run at the same
  * time on one GPU, such as calls on two unordered streams, race on it.

@@ -99,6 +99,16 @@ def test_small_and_irregular_shapes(hc, shape, rows, dt):
     check(hc, rows, C, H, R, dt, seed=3)
 
 
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+@pytest.mark.parametrize("rows", [9, 12, 16])
+def test_real_shape_decode_up_to_16_rows(hc, dt, rows):
+    """The tensor-core decode pair serves up to 16 rows (the MMA's N) where a
+    CTA of each kernel still shares an SM at 16 rows: C = 4, H = 2560 does
+    (decode at 9-16 rows), C = 8, H = 1280 does not (prefill from 9 rows)."""
+    check(hc, rows, 4, 2560, 320, dt, expect_path=hc.HC_PATH_DECODE)
+    check(hc, rows, 8, 1280, 320, dt, seed=3, expect_path=hc.HC_PATH_PREFILL)
+
+
 # ---------------------------------------------- general path, more rows --
 
 @pytest.mark.parametrize("dt", ["bf16", "f16", "f32"])
@@ -123,7 +133,8 @@ def test_prefill_full_size_every_row(hc, dt, C, H):
 
 # ----------------------------------------------------------- invariants --
 
-@pytest.mark.parametrize("rows,flags", [(8, 0), (8, 2), (40, 2)], ids=["decode", "general", "general40"])
+@pytest.mark.parametrize("rows,flags", [(8, 0), (16, 0), (8, 2), (40, 2)],
+                         ids=["decode", "decode16", "general", "general40"])
 def test_row_independence_bitwise(hc, rows, flags):
     """A row gives the same bits at any batch size, within one path."""
     C, H, R = 4, 2560, 320
@@ -354,12 +365,12 @@ def test_workspace_errors(hc):
     assert e.value.status == 3
 
 
-@pytest.mark.parametrize("small,large,dt", [(8, 9, "bf16"), (8, 9, "f16"), (512, 513, "bf16"), (512, 513, "f16")],
+@pytest.mark.parametrize("small,large,dt", [(16, 17, "bf16"), (16, 17, "f16"), (512, 513, "bf16"), (512, 513, "f16")],
                          ids=["decode8-prefill9-bf16", "decode8-prefill9-f16", "prefill512-513-bf16",
                               "prefill512-513-f16"])
 def test_row_bits_across_batch_size_switches(hc, small, large, dt):
     """The same rows in a batch just below and just above a switch of the
-    path (8 -> 9 rows: decode -> prefill) or of the prefill path's K split
+    path (16 -> 17 rows: decode -> prefill) or of the prefill path's K split
     (512 -> 513 rows: 256-wide slices -> branch-wide slices). Both sides meet
     the oracle tolerance (tested above); here the difference between them is
     measured and bounded: streams_out identical, most pre_output elements
@@ -444,7 +455,7 @@ PREFILL_SHAPES = [(4, 2560, 320), (8, 1280, 320), (1, 4096, 64), (2, 128, 64), (
 
 
 @pytest.mark.parametrize("shape", PREFILL_SHAPES, ids=lambda s: "C%d_H%d_R%d" % s)
-@pytest.mark.parametrize("rows", [9, 130, 300])
+@pytest.mark.parametrize("rows", [17, 130, 300])
 @pytest.mark.parametrize("dt", ["bf16", "f16"])
 def test_prefill_path_shapes(hc, shape, rows, dt):
     """tcgen05 path: one partial tile, several tiles with a ragged tail."""

@@ -87,8 +87,8 @@ def test_refuses_problems_beyond_the_static_scratch(api):
     out = (t(rows, H), t(rows, C), t(rows, C * H))
     assert call_noalloc(B, f, g, rows, C, H, R, out, I.QWEN_ATTRS) == 2   # HC_ERR_UNSUPPORTED
     assert b"scratch" in B.lib().hc_last_error()
-    # more than 8 rows is not a decode-path problem
-    rows = 9
+    # more than 16 rows is not a decode-path problem
+    rows = 17
     C, H, R = 4, 256, 32
     g = dict(streams=t(rows, C * H), norm_scale=t(C * H), down_w=t(C * H, R), up_w=t(R, C * H),
              inject_w=t(C * H, C), prev_out=t(rows, H), prev_gate=t(rows, C))
