@@ -165,7 +165,7 @@ __device__ __forceinline__ uint32_t idesc_t() {
 // memory), 4 inverse RMS stored, 5 weights landed, 6 MMA operands ready, 7 MMA
 // done, 8 cluster exchange landed, 9 partial sums written.
 template <typename T, int MB, bool TIMED = false>
-__global__ void __maxnreg__(64) dec_down_um(const __grid_constant__ DownArgs<T> a) {
+__global__ void __maxnreg__(MB > 8 ? 72 : 64) dec_down_um(const __grid_constant__ DownArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int VEC = 8;
@@ -612,7 +612,7 @@ __device__ __noinline__ void dec_post_gate_ws(const float* inj, int B, int C, in
 // wait), 2 wait returned, 3 partial sums landed, 4 MMA operands ready, 5 MMA
 // done, 6 pre-mix products landed, 7 pre_output written.
 template <typename T, int MB, bool TIMED = false>
-__global__ void __launch_bounds__(512) dec_up_um(const UpArgs<T> a) {
+__global__ void __launch_bounds__(512, (MB > 8 ? 1 : 2)) dec_up_um(const UpArgs<T> a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   constexpr int VEC = 8, HS = kUpHS;
