@@ -785,21 +785,33 @@ __global__ void __launch_bounds__(512, (MB > 8 ? 1 : 2)) dec_up_um(const UpArgs<
       *reinterpret_cast<T*>(sB + b_off(b, col)) = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x), a.at.alpha) : qnan);
     }
   }
-  if constexpr (MB > 1) if (split) {
-    const int npair = ncols / 2;
+  if constexpr (MB > 1) if (split && d_thread) {
+    // one column per thread; lanes 2k and 2k + 1 hold columns lc and lc + 1
+    // of one row (ncols and nthr_d are even), swap their values to form the
+    // contiguous pair and send it to half of the ranks each
+    const int total = B * ncols;
     const size_t stride = static_cast<size_t>(B) * a.per;
     #pragma unroll 1
-    for (int i = d_thread ? tid : B * npair; i < B * npair; i += nthr_d) {
-      const int b = i / npair, lc = 2 * (i - b * npair);
-      const float* src = st + static_cast<size_t>(b) * a.per + lc;
-      const float x0 = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
-      const float x1 = ordered_sum(NCLU, [&](int p) { return src[p * stride + 1]; });
-      T dv[2];
-      dv[0] = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x0), a.at.alpha) : qnan);
-      dv[1] = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x1), a.at.alpha) : qnan);
-      const uint32_t packed = *reinterpret_cast<const uint32_t*>(dv);
-      const uint32_t slot = smem_addr(sB + b_off(b, rank * a.per + lc));  // an even column pair is contiguous
-      for (int pr = 0; pr < SR; ++pr) st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
+    for (int wb = tid - lane; wb < total; wb += nthr_d) {  // warp-uniform: every lane reaches the shuffle
+      const int i = wb + lane;
+      const bool act = i < total;
+      const int b = act ? i / ncols : 0, lc = act ? i - b * ncols : 0;
+      float x = 0.0f;
+      if (act) {
+        const float* src = st + static_cast<size_t>(b) * a.per + lc;
+        x = ordered_sum(NCLU, [&](int p) { return src[p * stride]; });
+      }
+      const T dv = Ty<T>::from_f(ok ? scaled_silu_t<T>(rT<T>(x), a.at.alpha) : qnan);
+      const uint32_t mine = *reinterpret_cast<const uint16_t*>(&dv);
+      const uint32_t other = __shfl_xor_sync(0xffffffffu, mine, 1);
+      if (act) {
+        const uint32_t packed = (lane & 1) ? (other | (mine << 16)) : (mine | (other << 16));
+        const int lc0 = lc & ~1;
+        const uint32_t slot = smem_addr(sB + b_off(b, rank * a.per + lc0));  // an even column pair is contiguous
+        const int half = SR / 2, r0 = (lane & 1) ? half : 0, r1 = (lane & 1) ? SR : half;
+        for (int pr = r0; pr < r1; ++pr)
+          st_async_b32(mapa_shared(slot, pr), packed, mapa_shared(smem_addr(dbar), pr));
+      }
     }
   }
   // The MMA may start once the d warps have written d and hn and every
