@@ -79,15 +79,15 @@ __host__ __device__ inline uint32_t b_off(int row, int k) { return static_cast<u
 // one row, (p, b, col) row-major with NCP columns: dec_up_um pulls the whole
 // array with one bulk copy. With more rows (split mode: SR up ranks, rank c
 // reducing the `per` down columns c*per.. and rank 0 the inject columns) the
-// down columns are grouped by the rank that consumes them, (p, rank, b,
+// down columns are grouped by the rank that consumes them, (rank, p, b,
 // per), followed by the inject columns as (p, b, 8): each rank pulls one
-// contiguous block per cluster and rank 0 one block of inject columns.
-// SR = 0 means no split.
+// contiguous block (every cluster's share of its columns) and rank 0 one
+// block of inject columns. SR = 0 means no split.
 __host__ __device__ inline int64_t part_index(int SR, int p, int b, int col, int B, int R, int NCP, int per, int NCLU) {
   if (SR == 0) return (static_cast<int64_t>(p) * B + b) * NCP + col;
   if (col < R) {
     const int rank = col / per;
-    return ((static_cast<int64_t>(p) * SR + rank) * B + b) * per + (col - rank * per);
+    return ((static_cast<int64_t>(rank) * NCLU + p) * B + b) * per + (col - rank * per);
   }
   return static_cast<int64_t>(NCLU) * SR * B * per + (static_cast<int64_t>(p) * B + b) * 8 + (col - R);
 }
@@ -748,13 +748,12 @@ __global__ void __launch_bounds__(512, (MB > 8 ? 1 : 2)) dec_up_um(const UpArgs<
     if (!split) {
       if (lane == 0) bulk_g2s(st, a.part_ws, bytes, bar);
     } else {
-      // one block of B * per partials per cluster for this rank, and (rank 0
-      // of the first column tile, up to 8 rows) one block of every cluster's
-      // inject partials
-      #pragma unroll 1
-      for (int p = lane; p < NCLU; p += 32)
-        bulk_g2s(st + static_cast<size_t>(p) * B * a.per,
-                 a.part_ws + (static_cast<int64_t>(p) * SR + rank) * B * a.per, static_cast<uint32_t>(B * a.per * 4), bar);
+      // one block of every cluster's B * per partials for this rank, and
+      // (rank 0 of the first column tile, up to 8 rows) one block of every
+      // cluster's inject partials
+      if (lane == 0)
+        bulk_g2s(st, a.part_ws + static_cast<int64_t>(rank) * NCLU * B * a.per,
+                 static_cast<uint32_t>(NCLU * B * a.per * 4), bar);
       if (kStageInj && do_post && lane == 0)
         bulk_g2s(st + inj_off, a.part_ws + static_cast<int64_t>(NCLU) * SR * B * a.per,
                  static_cast<uint32_t>(NCLU * B * 32), bar);
