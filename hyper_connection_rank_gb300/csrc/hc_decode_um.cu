@@ -433,9 +433,27 @@ __global__ void __maxnreg__(MB > 8 ? 72 : 64) dec_down_um(const __grid_constant_
   // One or two rows: the inverse RMS once per thread, before the weights are
   // waited for, and one thread per K row of the slice for hn (no division)
   float inv2[2] = {0.0f, 0.0f};
-  if constexpr (MB <= 2) {
+  if constexpr (MB == 1) {
     inv2[0] = inv_of(0);
-    if (MB == 2 && B == 2) inv2[1] = inv_of(1);
+  } else if constexpr (MB == 2) {
+    if (xmode) {
+      inv2[0] = wsum[0];
+      inv2[1] = wsum[1];
+    } else {
+      // both rows at once: the 24 warp sums loaded together (wsum is
+      // [warp][row]), the two sums added in warp order side by side
+      float2 x[kDownWarps];
+#pragma unroll
+      for (int w = 0; w < kDownWarps; ++w) x[w] = reinterpret_cast<const float2*>(wsum)[w];
+      float t0 = 0.0f, t1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kDownWarps; ++w) {
+        t0 += x[w].x;
+        t1 += x[w].y;
+      }
+      inv2[0] = inv_rms(t0, H, a.eps);
+      inv2[1] = inv_rms(t1, H, a.eps);
+    }
   }
   if (hk0 == 0 && tid < B) a.inv_ws[tid * C + c] = MB <= 2 ? (tid == 0 ? inv2[0] : inv2[1]) : inv_of(tid);
   HC_PHASE(4);
